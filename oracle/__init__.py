@@ -1,0 +1,168 @@
+"""CPU oracle for the BRA forward (test infrastructure).
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+import this package. It wraps the double-precision C implementation in
+`bra_oracle.c` through ctypes; arrays are numpy float64 (inputs are widened
+exactly from float32 / bfloat16 values).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bra_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into oracle/liboracle.so."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-Wall", "-Wextra", "-o", tmp, _SRC,
+                               "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        sig = {
+            "oracle_region_means": [P, I, I, I, I, I, P],
+            "oracle_affinity": [P, P, I, I, I, I, I, P],
+            "oracle_topk": [P, I, I, I, P],
+            "oracle_route": [P, P, I, I, I, I, I, I, P, P],
+            "oracle_routed_attention": [P, P, P, P, I, I, I, I, I, I, I, P, I],
+            "oracle_query_probs": [P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, P, P, P],
+            "oracle_lepe": [P, I, I, I, I, P, P, I, P],
+            "oracle_attend": [P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, I],
+            "oracle_forward": [P, P, P, I, I, I, I, I, I, I, P, P, I, P, P, I],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"{what}: invalid argument (status {rc})")
+
+
+def region_means(x, S: int) -> np.ndarray:
+    x = _f64(x)
+    B, H, W, C = x.shape
+    out = np.empty((B, S * S, C))
+    _check(_load().oracle_region_means(_p(x), B, H, W, C, S, _p(out)), "region_means")
+    return out
+
+
+def affinity(q, k, S: int) -> np.ndarray:
+    q, k = _f64(q), _f64(k)
+    B, H, W, C = q.shape
+    A = np.empty((B, S * S, S * S))
+    _check(_load().oracle_affinity(_p(q), _p(k), B, H, W, C, S, _p(A)), "affinity")
+    return A
+
+
+def topk(A, topk: int) -> np.ndarray:
+    """Top-k of each row of A (last axis), largest first, ties to lowest index."""
+    A = _f64(A)
+    R = A.shape[-1]
+    rows = int(np.prod(A.shape[:-1]))
+    idx = np.empty(A.shape[:-1] + (topk,), dtype=np.int32)
+    _check(_load().oracle_topk(_p(A), rows, R, topk, _p(idx)), "topk")
+    return idx
+
+
+def route(q, k, S: int, topk: int):
+    """Returns (idx [B, S*S, topk] int32, affinity [B, S*S, S*S] float64)."""
+    q, k = _f64(q), _f64(k)
+    B, H, W, C = q.shape
+    idx = np.empty((B, S * S, topk), dtype=np.int32)
+    A = np.empty((B, S * S, S * S))
+    _check(_load().oracle_route(_p(q), _p(k), B, H, W, C, S, topk, _p(idx), _p(A)), "route")
+    return idx, A
+
+
+def routed_attention(q, k, v, idx, heads: int, S: int, threads: int = 1) -> np.ndarray:
+    q, k, v, idx = _f64(q), _f64(k), _f64(v), _i32(idx)
+    B, H, W, C = q.shape
+    out = np.empty_like(q)
+    _check(_load().oracle_routed_attention(_p(q), _p(k), _p(v), _p(idx), B, H, W, C,
+                                           heads, S, idx.shape[-1], _p(out), threads),
+           "routed_attention")
+    return out
+
+
+def query_probs(q, k, v, idx, heads: int, S: int, b: int, y: int, x: int, h: int):
+    """(probs [k*n], key token ids y*W+x [k*n], out [d]) of one query."""
+    q, k, v, idx = _f64(q), _f64(k), _f64(v), _i32(idx)
+    B, H, W, C = q.shape
+    topk = idx.shape[-1]
+    n = (H // S) * (W // S)
+    probs = np.empty(topk * n)
+    keys = np.empty(topk * n, dtype=np.int32)
+    out = np.empty(C // heads)
+    _check(_load().oracle_query_probs(_p(q), _p(k), _p(v), _p(idx), B, H, W, C, heads, S,
+                                      topk, b, y, x, h, _p(probs), _p(keys), _p(out)),
+           "query_probs")
+    return probs, keys, out
+
+
+def lepe(v, w, bias) -> np.ndarray:
+    v, w = _f64(v), _f64(w)
+    bias = None if bias is None else _f64(bias)
+    B, H, W, C = v.shape
+    out = np.empty_like(v)
+    _check(_load().oracle_lepe(_p(v), B, H, W, C, _p(w), _p(bias), w.shape[-1], _p(out)),
+           "lepe")
+    return out
+
+
+def attend(q, k, v, idx, heads: int, S: int, w, bias, threads: int = 1) -> np.ndarray:
+    q, k, v, idx, w = _f64(q), _f64(k), _f64(v), _i32(idx), _f64(w)
+    bias = None if bias is None else _f64(bias)
+    B, H, W, C = q.shape
+    out = np.empty_like(q)
+    _check(_load().oracle_attend(_p(q), _p(k), _p(v), _p(idx), B, H, W, C, heads, S,
+                                 idx.shape[-1], _p(w), _p(bias), w.shape[-1], _p(out),
+                                 threads), "attend")
+    return out
+
+
+def forward(q, k, v, heads: int, S: int, topk: int, w, bias, threads: int = 1):
+    """Returns (out [B, H, W, C] float64, idx [B, S*S, topk] int32)."""
+    q, k, v, w = _f64(q), _f64(k), _f64(v), _f64(w)
+    bias = None if bias is None else _f64(bias)
+    B, H, W, C = q.shape
+    out = np.empty_like(q)
+    idx = np.empty((B, S * S, topk), dtype=np.int32)
+    _check(_load().oracle_forward(_p(q), _p(k), _p(v), B, H, W, C, heads, S, topk,
+                                  _p(w), _p(bias), w.shape[-1], _p(idx), _p(out), threads),
+           "forward")
+    return out, idx

@@ -1,0 +1,390 @@
+/*
+ * bra_oracle.c -- CPU oracle for the forward pass of Bi-Level Routing
+ * Attention (BRA), the attention of BiFormer.
+ *
+ * TEST INFRASTRUCTURE. This is the plain, slow, double-precision definition
+ * the CUDA library is checked against. Only the test suite, the smoke check and
+ * the CPU-baseline leg of the benchmark load it; the library never does, and
+ * this file shares no code, header or table with the CUDA sources.
+ *
+ * Sources (web pages about BiFormer; each function cites the passage it
+ * follows):
+ *   [P1] "CVPR2023：BiFormer中的双层路由注意力机制解析" (cybasar.com),
+ *        §2 (region-level routing idea) and §3 (implementation steps).
+ *   [P2] "从静态到动态：BRA双层路由注意力如何革新视觉Transformer的计算范式"
+ *        (snabindia.com), §2 (region mean pooling), §4 (TopkRouting, LePE).
+ *   [P4] "Biformer注意力机制的原理及数学公式推导" (csdn), the local-window
+ *        attention formula softmax(Q K^T / sqrt(d_k)) V.
+ *   [P5] "BiFormer: Vision Transformer mit Bi-Level-Routing-Attention"
+ *        (hyper.ai, arXiv 2303.08810 abstract): token-to-token attention over
+ *        the union of the routed regions.
+ *
+ * Readings where the pages leave a step open (all stated in the design notes):
+ *   - Regions are numbered row-major on the S x S grid and tokens row-major
+ *     inside a region, which is what [P1] §3's reshape to [S^2, HW/S^2, C]
+ *     produces. H and W must be multiples of S.
+ *   - Routing uses all C channels (one routing per image shared by the heads),
+ *     as [P1] §3 gives q_r the shape [S^2, C]. The affinity is unscaled (a
+ *     positive scale does not change the order).
+ *   - Top-k: largest values first, ties to the lowest region index.
+ *   - Head h owns channels [h*d, (h+1)*d), d = C / heads; the attention scale
+ *     is d^-1/2 (the key dimension of [P4]'s formula).
+ *   - One softmax per query over all k*n routed keys jointly ([P1] §3's k_g
+ *     has k*HW/S^2 keys per region and the softmax runs over the last axis).
+ *   - LePE is the depthwise (groups = C) cross-correlation of V with a
+ *     ks x ks kernel and a bias, zero-padded by ks/2 at the image border
+ *     ([P2] §4's nn.Conv2d(dim, dim, ks, stride 1, padding ks//2,
+ *     groups=dim)), added to the attention output ([P1] §3 `out += lce(v)`).
+ *     No residual and no output projection.
+ *
+ * All tensors are contiguous channels-last [B, H, W, C] arrays of double.
+ * Functions return 0 on success and 1 on an invalid argument.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+
+typedef struct {
+  int B, H, W, C, S;
+  int R;      /* regions per image, S*S */
+  int hr, wr; /* region height and width in tokens */
+  int n;      /* tokens per region */
+} geom;
+
+static int make_geom(int B, int H, int W, int C, int S, geom *g) {
+  if (B < 0 || H <= 0 || W <= 0 || C <= 0 || S <= 0) return ORACLE_EINVAL;
+  if (H % S || W % S) return ORACLE_EINVAL;
+  g->B = B; g->H = H; g->W = W; g->C = C; g->S = S;
+  g->R = S * S;
+  g->hr = H / S;
+  g->wr = W / S;
+  g->n = g->hr * g->wr;
+  return ORACLE_OK;
+}
+
+/* Region partition, [P1] §3: token t of region r (row-major grid of S x S
+ * regions, row-major tokens inside a region) sits at image row y, column x. */
+static void region_token(const geom *g, int r, int t, int *y, int *x) {
+  int ry = r / g->S, rx = r % g->S;
+  *y = ry * g->hr + t / g->wr;
+  *x = rx * g->wr + t % g->wr;
+}
+
+static size_t offset_of(const geom *g, int b, int y, int x) {
+  return (((size_t)b * g->H + y) * g->W + x) * (size_t)g->C;
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 1: region-level mean of a token map ([P1] §3 `q.mean(dim=1)`; [P2] §2
+ * pools each region by its average). out is [B, S*S, C].
+ */
+int oracle_region_means(const double *x, int B, int H, int W, int C, int S,
+                        double *out) {
+  geom g;
+  if (!x || !out || make_geom(B, H, W, C, S, &g)) return ORACLE_EINVAL;
+  for (int b = 0; b < B; ++b)
+    for (int r = 0; r < g.R; ++r)
+      for (int c = 0; c < C; ++c) {
+        double sum = 0.0;
+        for (int t = 0; t < g.n; ++t) {
+          int y, xx;
+          region_token(&g, r, t, &y, &xx);
+          sum += x[offset_of(&g, b, y, xx) + c];
+        }
+        out[((size_t)b * g.R + r) * C + c] = sum / g.n;
+      }
+  return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 2: region affinity A_r = q_r k_r^T over all C channels ([P1] §3;
+ * [P2] §4 TopkRouting's attn_logit, without the positive scale). A is
+ * [B, S*S, S*S].
+ */
+int oracle_affinity(const double *q, const double *k, int B, int H, int W,
+                    int C, int S, double *A) {
+  geom g;
+  if (!q || !k || !A || make_geom(B, H, W, C, S, &g)) return ORACLE_EINVAL;
+  size_t nm = (size_t)B * g.R * C;
+  double *qm = malloc(nm * sizeof(double));
+  double *km = malloc(nm * sizeof(double));
+  if (!qm || !km) { free(qm); free(km); return ORACLE_EINVAL; }
+  oracle_region_means(q, B, H, W, C, S, qm);
+  oracle_region_means(k, B, H, W, C, S, km);
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < g.R; ++i)
+      for (int j = 0; j < g.R; ++j) {
+        const double *qi = qm + ((size_t)b * g.R + i) * C;
+        const double *kj = km + ((size_t)b * g.R + j) * C;
+        double dot = 0.0;
+        for (int c = 0; c < C; ++c) dot += qi[c] * kj[c];
+        A[((size_t)b * g.R + i) * g.R + j] = dot;
+      }
+  free(qm);
+  free(km);
+  return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 3: per-row top-k of the affinity ([P1] §3 `torch.topk(A_r, k).indices`;
+ * [P2] §4). Largest first; among equal values the lowest column wins. A is
+ * [rows, R]; idx is [rows, topk].
+ */
+int oracle_topk(const double *A, int rows, int R, int topk, int32_t *idx) {
+  if (!A || !idx || rows < 0 || R <= 0 || topk <= 0 || topk > R)
+    return ORACLE_EINVAL;
+  unsigned char *taken = malloc((size_t)R);
+  if (!taken) return ORACLE_EINVAL;
+  for (int i = 0; i < rows; ++i) {
+    const double *row = A + (size_t)i * R;
+    memset(taken, 0, (size_t)R);
+    for (int m = 0; m < topk; ++m) {
+      int best = -1;
+      for (int j = 0; j < R; ++j) {
+        if (taken[j]) continue;
+        if (best < 0 || row[j] > row[best]) best = j; /* strict: ties keep lower j */
+      }
+      taken[best] = 1;
+      idx[(size_t)i * topk + m] = best;
+    }
+  }
+  free(taken);
+  return ORACLE_OK;
+}
+
+/* Routing = steps 1-3. idx is [B, S*S, topk]; A (optional) is [B, S*S, S*S]. */
+int oracle_route(const double *q, const double *k, int B, int H, int W, int C,
+                 int S, int topk, int32_t *idx, double *A_out) {
+  geom g;
+  if (!q || !k || !idx || make_geom(B, H, W, C, S, &g)) return ORACLE_EINVAL;
+  if (topk <= 0 || topk > g.R) return ORACLE_EINVAL;
+  size_t na = (size_t)B * g.R * g.R;
+  double *A = A_out ? A_out : malloc((na ? na : 1) * sizeof(double));
+  if (!A) return ORACLE_EINVAL;
+  int rc = oracle_affinity(q, k, B, H, W, C, S, A);
+  if (!rc) rc = oracle_topk(A, B * g.R, g.R, topk, idx);
+  if (!A_out) free(A);
+  return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 4: token-to-token attention over the routed regions ([P1] §3: gather
+ * k and v of the k routed regions, attn = softmax(q k_g^T * scale), out =
+ * attn v_g; [P5]: attention over the union of the routed regions; [P4]: scale
+ * 1/sqrt(d_k)). The gathered keys are never stored here either: each query
+ * walks the routed regions directly.
+ */
+typedef struct {
+  const double *q, *k, *v;
+  const int32_t *idx;
+  geom g;
+  int heads, topk;
+  double *out;
+  int status;
+} attn_job;
+
+/* Logits, probabilities and output of one query (b, region i, slot t, head h).
+ * probs / keys (optional) receive the k*n probabilities and the flat token
+ * index y*W + x of each key, in routed order. */
+static int attend_one(const attn_job *J, int b, int i, int t, int h,
+                      double *logit, double *probs, int32_t *keys,
+                      double *out_vec) {
+  const geom *g = &J->g;
+  int d = g->C / J->heads;
+  double scale = 1.0 / sqrt((double)d);
+  int y, x;
+  region_token(g, i, t, &y, &x);
+  const double *qv = J->q + offset_of(g, b, y, x) + (size_t)h * d;
+  int nk = J->topk * g->n;
+  for (int m = 0; m < J->topk; ++m) {
+    int j = J->idx[((size_t)b * g->R + i) * J->topk + m];
+    if (j < 0 || j >= g->R) return ORACLE_EINVAL;
+    for (int s = 0; s < g->n; ++s) {
+      int yk, xk;
+      region_token(g, j, s, &yk, &xk);
+      const double *kv = J->k + offset_of(g, b, yk, xk) + (size_t)h * d;
+      double dot = 0.0;
+      for (int e = 0; e < d; ++e) dot += qv[e] * kv[e];
+      logit[m * g->n + s] = dot * scale;
+      if (keys) keys[m * g->n + s] = yk * g->W + xk;
+    }
+  }
+  /* softmax over all nk keys jointly: subtract the max, exponentiate, divide */
+  double mx = logit[0];
+  for (int a = 1; a < nk; ++a) if (logit[a] > mx) mx = logit[a];
+  double sum = 0.0;
+  for (int a = 0; a < nk; ++a) { logit[a] = exp(logit[a] - mx); sum += logit[a]; }
+  for (int a = 0; a < nk; ++a) logit[a] /= sum;
+  if (probs) memcpy(probs, logit, (size_t)nk * sizeof(double));
+  if (out_vec) {
+    for (int e = 0; e < d; ++e) out_vec[e] = 0.0;
+    for (int m = 0; m < J->topk; ++m) {
+      int j = J->idx[((size_t)b * g->R + i) * J->topk + m];
+      for (int s = 0; s < g->n; ++s) {
+        int yk, xk;
+        region_token(g, j, s, &yk, &xk);
+        const double *vv = J->v + offset_of(g, b, yk, xk) + (size_t)h * d;
+        double p = logit[m * g->n + s];
+        for (int e = 0; e < d; ++e) out_vec[e] += p * vv[e];
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+typedef struct {
+  attn_job *job;
+  int tid, nthreads;
+} attn_worker;
+
+static void *attn_thread(void *arg) {
+  attn_worker *w = (attn_worker *)arg;
+  attn_job *J = w->job;
+  const geom *g = &J->g;
+  int d = g->C / J->heads;
+  double *logit = malloc((size_t)J->topk * g->n * sizeof(double));
+  if (!logit) { J->status = ORACLE_EINVAL; return NULL; }
+  long units = (long)g->B * g->R;
+  for (long u = w->tid; u < units; u += w->nthreads) {
+    int b = (int)(u / g->R), i = (int)(u % g->R);
+    for (int t = 0; t < g->n; ++t) {
+      int y, x;
+      region_token(g, i, t, &y, &x);
+      for (int h = 0; h < J->heads; ++h) {
+        double *o = J->out + offset_of(g, b, y, x) + (size_t)h * d;
+        if (attend_one(J, b, i, t, h, logit, NULL, NULL, o))
+          J->status = ORACLE_EINVAL;
+      }
+    }
+  }
+  free(logit);
+  return NULL;
+}
+
+static int run_threads(void *(*fn)(void *), attn_job *job, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  attn_worker *ws = malloc(sizeof(attn_worker) * (size_t)nthreads);
+  pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!ws || !th) { free(ws); free(th); return ORACLE_EINVAL; }
+  for (int t = 0; t < nthreads; ++t) {
+    ws[t].job = job; ws[t].tid = t; ws[t].nthreads = nthreads;
+  }
+  for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, fn, &ws[t]);
+  fn(&ws[0]);
+  for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(ws);
+  free(th);
+  return ORACLE_OK;
+}
+
+static int attn_args_ok(const double *q, const double *k, const double *v,
+                        const int32_t *idx, int B, int H, int W, int C,
+                        int heads, int S, int topk, geom *g) {
+  if (!q || !k || !v || !idx || make_geom(B, H, W, C, S, g)) return 0;
+  if (heads <= 0 || C % heads) return 0;
+  if (topk <= 0 || topk > g->R) return 0;
+  return 1;
+}
+
+/* Attention part only: out[B, H, W, C] = routed softmax attention. */
+int oracle_routed_attention(const double *q, const double *k, const double *v,
+                            const int32_t *idx, int B, int H, int W, int C,
+                            int heads, int S, int topk, double *out,
+                            int nthreads) {
+  attn_job J;
+  if (!out || !attn_args_ok(q, k, v, idx, B, H, W, C, heads, S, topk, &J.g))
+    return ORACLE_EINVAL;
+  J.q = q; J.k = k; J.v = v; J.idx = idx;
+  J.heads = heads; J.topk = topk; J.out = out; J.status = ORACLE_OK;
+  if (run_threads(attn_thread, &J, nthreads)) return ORACLE_EINVAL;
+  return J.status;
+}
+
+/* Probabilities of one query: probs[topk*n], keys[topk*n] (flat y*W + x),
+ * out_vec[d] (optional). Used by the softmax-sum and order checks. */
+int oracle_query_probs(const double *q, const double *k, const double *v,
+                       const int32_t *idx, int B, int H, int W, int C,
+                       int heads, int S, int topk, int b, int y, int x, int h,
+                       double *probs, int32_t *keys, double *out_vec) {
+  attn_job J;
+  if (!probs || !attn_args_ok(q, k, v, idx, B, H, W, C, heads, S, topk, &J.g))
+    return ORACLE_EINVAL;
+  if (b < 0 || b >= B || y < 0 || y >= H || x < 0 || x >= W || h < 0 ||
+      h >= heads)
+    return ORACLE_EINVAL;
+  J.q = q; J.k = k; J.v = v; J.idx = idx;
+  J.heads = heads; J.topk = topk; J.out = NULL; J.status = ORACLE_OK;
+  const geom *g = &J.g;
+  int i = (y / g->hr) * g->S + x / g->wr;
+  int t = (y % g->hr) * g->wr + x % g->wr;
+  double *logit = malloc((size_t)topk * g->n * sizeof(double));
+  if (!logit) return ORACLE_EINVAL;
+  int rc = attend_one(&J, b, i, t, h, logit, probs, keys, out_vec);
+  free(logit);
+  return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 5: LePE ([P2] §4: nn.Conv2d(dim, dim, kernel_size=ks, stride=1,
+ * padding=ks//2, groups=dim) applied to V; bias included as nn.Conv2d's
+ * default). Cross-correlation, zero padding at the image border.
+ * w is [C, ks, ks], bias [C] or NULL (zero). out is [B, H, W, C].
+ */
+int oracle_lepe(const double *v, int B, int H, int W, int C, const double *w,
+                const double *bias, int ks, double *out) {
+  if (!v || !w || !out || B < 0 || H <= 0 || W <= 0 || C <= 0) return ORACLE_EINVAL;
+  if (ks <= 0 || ks % 2 == 0) return ORACLE_EINVAL;
+  int pad = ks / 2;
+  for (int b = 0; b < B; ++b)
+    for (int y = 0; y < H; ++y)
+      for (int x = 0; x < W; ++x)
+        for (int c = 0; c < C; ++c) {
+          double acc = bias ? bias[c] : 0.0;
+          for (int u = 0; u < ks; ++u)
+            for (int s = 0; s < ks; ++s) {
+              int yy = y + u - pad, xx = x + s - pad;
+              if (yy < 0 || yy >= H || xx < 0 || xx >= W) continue;
+              acc += w[((size_t)c * ks + u) * ks + s] *
+                     v[(((size_t)b * H + yy) * W + xx) * C + c];
+            }
+          out[(((size_t)b * H + y) * W + x) * C + c] = acc;
+        }
+  return ORACLE_OK;
+}
+
+/* Attend = step 4 + step 5 (out = attention + LePE(v)), given the routing. */
+int oracle_attend(const double *q, const double *k, const double *v,
+                  const int32_t *idx, int B, int H, int W, int C, int heads,
+                  int S, int topk, const double *w, const double *bias, int ks,
+                  double *out, int nthreads) {
+  geom g;
+  if (!out || !w || !attn_args_ok(q, k, v, idx, B, H, W, C, heads, S, topk, &g))
+    return ORACLE_EINVAL;
+  size_t total = (size_t)B * H * W * C;
+  double *lepe = malloc((total ? total : 1) * sizeof(double));
+  if (!lepe) return ORACLE_EINVAL;
+  int rc = oracle_routed_attention(q, k, v, idx, B, H, W, C, heads, S, topk,
+                                   out, nthreads);
+  if (!rc) rc = oracle_lepe(v, B, H, W, C, w, bias, ks, lepe);
+  if (!rc)
+    for (size_t e = 0; e < total; ++e) out[e] += lepe[e];
+  free(lepe);
+  return rc;
+}
+
+/* The whole forward: routing (steps 1-3), then attend (steps 4-5). */
+int oracle_forward(const double *q, const double *k, const double *v, int B,
+                   int H, int W, int C, int heads, int S, int topk,
+                   const double *w, const double *bias, int ks, int32_t *idx,
+                   double *out, int nthreads) {
+  int rc = oracle_route(q, k, B, H, W, C, S, topk, idx, NULL);
+  if (rc) return rc;
+  return oracle_attend(q, k, v, idx, B, H, W, C, heads, S, topk, w, bias, ks,
+                       out, nthreads);
+}

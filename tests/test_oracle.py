@@ -1,0 +1,349 @@
+"""Pins for the CPU oracle: closed forms, special cases that reduce to library
+routines, invariants and a hand-derived worked example.
+
+None of these re-types the oracle's code: each check computes the expected
+value another way (numpy / torch CPU library routines in float64, closed
+forms, or constructions whose answer follows from the mathematics).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import bra_synth
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+
+def region_tokens_per_page(H, W, S):
+    """Token ids y*W+x of each region, built the way the BRA write-up
+    partitions the map: reshape (S, H/S, S, W/S) then swap the two middle
+    axes, giving [S^2, HW/S^2] (page "CVPR2023：BiFormer中的双层路由注意力机制解析",
+    section 3)."""
+    ids = np.arange(H * W).reshape(S, H // S, S, W // S)
+    return ids.transpose(0, 2, 1, 3).reshape(S * S, (H // S) * (W // S))
+
+
+def rand_map(B, H, W, C, scale=1.0):
+    return RNG.standard_normal((B, H, W, C)) * scale
+
+
+def sdpa_heads(q, k, v, heads, mask=None):
+    """Multi-head softmax(QK^T/sqrt(d))V over token sequences with torch
+    (float64, CPU). q,k,v: [B, N, C]; mask: [B, N, N] bool (True = attend)."""
+    B, N, C = q.shape
+    d = C // heads
+    t = lambda a: torch.from_numpy(a).reshape(B, N, heads, d).transpose(1, 2)
+    m = None if mask is None else torch.from_numpy(mask)[:, None]
+    o = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), attn_mask=m)
+    return o.transpose(1, 2).reshape(B, N, C).numpy()
+
+
+# --------------------------------------------------------------------------
+# Region means
+# --------------------------------------------------------------------------
+
+def test_region_means_closed_form_zero_noise():
+    wl = bra_synth.Workload("t", 2, 12, 8, 16, 2, 4, 2, 3, "f32")
+    x = bra_synth.make_inputs(wl, seed=3, noise_std=0.0)
+    means = oracle.region_means(x.q, wl.S)
+    # with no per-token noise every token of a region holds the region offset
+    regs = region_tokens_per_page(wl.H, wl.W, wl.S)
+    flat = x.q.reshape(wl.B, wl.H * wl.W, wl.C).astype(np.float64)
+    for r in range(wl.R):
+        np.testing.assert_array_equal(means[:, r], flat[:, regs[r, 0]])
+        np.testing.assert_array_equal(means[:, r], flat[:, regs[r, -1]])
+
+
+def test_region_means_library_mean_over_page_partition():
+    B, H, W, C, S = 2, 12, 9, 5, 3
+    x = rand_map(B, H, W, C)
+    regs = region_tokens_per_page(H, W, S)
+    ref = x.reshape(B, H * W, C)[:, regs].mean(axis=2)
+    np.testing.assert_allclose(oracle.region_means(x, S), ref, rtol=0, atol=1e-13)
+    # the mean of the region means is the mean of all tokens (equal sizes)
+    np.testing.assert_allclose(oracle.region_means(x, S).mean(axis=1),
+                               x.reshape(B, -1, C).mean(axis=1), atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Affinity and top-k routing
+# --------------------------------------------------------------------------
+
+def test_affinity_closed_form_one_hot_offsets():
+    """Region offsets a_i e_{pi(i)} for q and b_j e_{sigma(j)} for k give
+    A[i, j] = a_i b_j [pi(i) == sigma(j)] exactly."""
+    B, S, hr, wr = 1, 3, 2, 2
+    H, W, R = S * hr, S * wr, S * S
+    C = R
+    pi, sigma = RNG.permutation(R), RNG.permutation(R)
+    a, b = RNG.integers(1, 9, R).astype(float), RNG.integers(1, 9, R).astype(float)
+    regs = region_tokens_per_page(H, W, S)
+    q = np.zeros((B, H * W, C))
+    k = np.zeros((B, H * W, C))
+    for r in range(R):
+        q[0, regs[r], pi[r]] = a[r]
+        k[0, regs[r], sigma[r]] = b[r]
+    A = oracle.affinity(q.reshape(B, H, W, C), k.reshape(B, H, W, C), S)
+    expect = np.where(pi[:, None] == sigma[None, :], a[:, None] * b[None, :], 0.0)
+    np.testing.assert_array_equal(A[0], expect)
+    idx, _ = oracle.route(q.reshape(B, H, W, C), k.reshape(B, H, W, C), S, 3)
+    # first pick is the one matching column; the rest are zero ties -> lowest j
+    for i in range(R):
+        j0 = int(np.nonzero(sigma == pi[i])[0][0])
+        rest = [j for j in range(R) if j != j0][:2]
+        assert list(idx[0, i]) == [j0] + rest
+
+
+def test_topk_matches_stable_argsort_with_ties():
+    for R, k in [(5, 1), (9, 4), (49, 16), (256, 4), (64, 64)]:
+        A = RNG.integers(-3, 4, size=(7, R)).astype(float)  # many ties
+        ref = np.argsort(-A, axis=-1, kind="stable")[:, :k]
+        np.testing.assert_array_equal(oracle.topk(A, k), ref)
+        A = RNG.standard_normal((7, R))
+        ref = np.argsort(-A, axis=-1, kind="stable")[:, :k]
+        np.testing.assert_array_equal(oracle.topk(A, k), ref)
+
+
+def test_topk_constant_row_takes_lowest_indices():
+    A = np.full((3, 10), 2.5)
+    np.testing.assert_array_equal(oracle.topk(A, 4), np.tile(np.arange(4), (3, 1)))
+
+
+def test_topk_brute_force_sets_tiny():
+    """The chosen set maximises the sum of affinities over all k-subsets."""
+    import itertools
+    for _ in range(20):
+        R, k = 6, 3
+        A = RNG.standard_normal((1, R))
+        best = max(itertools.combinations(range(R), k), key=lambda s: A[0, list(s)].sum())
+        assert set(oracle.topk(A, k)[0]) == set(best)
+
+
+def test_self_route_by_cauchy_schwarz():
+    """q = k with equal-norm, pairwise non-parallel region offsets and no
+    token noise: A[i, i] = |o|^2 > o_i . o_j, so every region routes to itself
+    first."""
+    B, S, hr, wr, C = 2, 4, 2, 3, 8
+    H, W, R = S * hr, S * wr, S * S
+    o = RNG.standard_normal((B, R, C))
+    o /= np.linalg.norm(o, axis=-1, keepdims=True)
+    regs = region_tokens_per_page(H, W, S)
+    x = np.zeros((B, H * W, C))
+    for r in range(R):
+        x[:, regs[r]] = o[:, r][:, None]
+    x = x.reshape(B, H, W, C)
+    idx, A = oracle.route(x, x, S, 1)
+    np.testing.assert_array_equal(idx[..., 0], np.tile(np.arange(R), (B, 1)))
+
+
+# --------------------------------------------------------------------------
+# Routed attention
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("heads", [1, 2, 4])
+def test_single_region_is_dense_attention(heads):
+    B, H, W, C = 2, 6, 5, 16
+    q, k, v = (rand_map(B, H, W, C) for _ in range(3))
+    idx = np.zeros((B, 1, 1), dtype=np.int32)
+    out = oracle.routed_attention(q, k, v, idx, heads, S=1)
+    ref = sdpa_heads(*(a.reshape(B, H * W, C) for a in (q, k, v)), heads)
+    np.testing.assert_allclose(out.reshape(B, H * W, C), ref, atol=1e-12)
+
+
+def test_all_regions_routed_is_dense_attention():
+    B, S, H, W, C, heads = 2, 3, 6, 9, 8, 2
+    q, k, v = (rand_map(B, H, W, C) for _ in range(3))
+    for _ in range(2):  # any order of the S^2 regions
+        idx = np.stack([np.stack([RNG.permutation(S * S) for _ in range(S * S)])
+                        for _ in range(B)]).astype(np.int32)
+        out = oracle.routed_attention(q, k, v, idx, heads, S)
+        ref = sdpa_heads(*(a.reshape(B, H * W, C) for a in (q, k, v)), heads)
+        np.testing.assert_allclose(out.reshape(B, H * W, C), ref, atol=1e-12)
+    # and through the full routing with topk = S^2
+    out, _ = oracle.forward(q, k, v, heads, S, S * S, np.zeros((C, 1, 1)), None)
+    np.testing.assert_allclose(out.reshape(B, H * W, C), ref, atol=1e-12)
+
+
+def test_routed_equals_masked_dense_attention():
+    B, S, H, W, C, heads, topk = 2, 4, 8, 12, 16, 4, 3
+    q, k, v = (rand_map(B, H, W, C) for _ in range(3))
+    idx = np.stack([np.stack([RNG.choice(S * S, topk, replace=False) for _ in range(S * S)])
+                    for _ in range(B)]).astype(np.int32)
+    regs = region_tokens_per_page(H, W, S)
+    tok_region = np.empty(H * W, dtype=int)
+    for r in range(S * S):
+        tok_region[regs[r]] = r
+    mask = np.zeros((B, H * W, H * W), dtype=bool)
+    for b in range(B):
+        for t in range(H * W):
+            mask[b, t] = np.isin(tok_region, idx[b, tok_region[t]])
+    ref = sdpa_heads(*(a.reshape(B, H * W, C) for a in (q, k, v)), heads, mask)
+    out = oracle.routed_attention(q, k, v, idx, heads, S)
+    np.testing.assert_allclose(out.reshape(B, H * W, C), ref, atol=1e-12)
+
+
+def test_window_attention_when_each_region_routes_to_itself():
+    """topk = 1 with self routing is non-overlapping window attention, the
+    local-window formula softmax(QK^T/sqrt(d_k))V inside each window (page
+    "Biformer注意力机制的原理及数学公式推导", local window attention)."""
+    B, S, hr, wr, C, heads = 1, 3, 4, 2, 8, 2
+    H, W = S * hr, S * wr
+    q, k, v = (rand_map(B, H, W, C) for _ in range(3))
+    idx = np.arange(S * S, dtype=np.int32).reshape(1, S * S, 1).repeat(B, 0)
+    out = oracle.routed_attention(q, k, v, idx, heads, S)
+    win = lambda a: a.reshape(B, S, hr, S, wr, C).transpose(0, 1, 3, 2, 4, 5).reshape(
+        B * S * S, hr * wr, C)
+    ref = sdpa_heads(win(q), win(k), win(v), heads)
+    ref = ref.reshape(B, S, S, hr, wr, C).transpose(0, 1, 3, 2, 4, 5).reshape(B, H, W, C)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+
+
+def test_softmax_rows_sum_to_one_and_order_invariance():
+    wl = bra_synth.WORKLOADS["tiny_f32"]
+    x = bra_synth.make_inputs(wl)
+    idx, _ = oracle.route(x.q, x.k, wl.S, wl.topk)
+    for (b, y, xx, h) in [(0, 0, 0, 0), (0, 13, 13, 1), (0, 5, 8, 0), (0, 7, 2, 1)]:
+        p, keys, _ = oracle.query_probs(x.q, x.k, x.v, idx, wl.heads, wl.S, b, y, xx, h)
+        assert p.shape == (wl.topk * wl.n,)
+        assert abs(p.sum() - 1.0) < 1e-12 and (p >= 0).all()
+        assert len(set(keys.tolist())) == len(keys)  # distinct routed regions
+    perm = idx[..., ::-1].copy()
+    a = oracle.routed_attention(x.q, x.k, x.v, idx, wl.heads, wl.S)
+    c = oracle.routed_attention(x.q, x.k, x.v, perm, wl.heads, wl.S)
+    np.testing.assert_allclose(a, c, atol=1e-12)
+
+
+def test_heads_are_independent_channel_blocks():
+    B, S, H, W, C, heads, topk = 1, 2, 4, 6, 12, 3, 2
+    q, k, v = (rand_map(B, H, W, C) for _ in range(3))
+    idx = np.stack([np.stack([RNG.choice(S * S, topk, replace=False) for _ in range(S * S)])
+                    for _ in range(B)]).astype(np.int32)
+    full = oracle.routed_attention(q, k, v, idx, heads, S)
+    d = C // heads
+    for h in range(heads):
+        sl = slice(h * d, (h + 1) * d)
+        part = oracle.routed_attention(q[..., sl], k[..., sl], v[..., sl], idx, 1, S)
+        np.testing.assert_allclose(full[..., sl], part, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# LePE
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ks", [1, 3, 5, 7])
+def test_lepe_is_depthwise_conv2d(ks):
+    B, H, W, C = 2, 9, 7, 6
+    v = rand_map(B, H, W, C)
+    w = RNG.standard_normal((C, ks, ks))
+    bias = RNG.standard_normal(C)
+    ref = torch.nn.functional.conv2d(torch.from_numpy(v).permute(0, 3, 1, 2),
+                                     torch.from_numpy(w)[:, None], torch.from_numpy(bias),
+                                     padding=ks // 2, groups=C).permute(0, 2, 3, 1).numpy()
+    np.testing.assert_allclose(oracle.lepe(v, w, bias), ref, atol=1e-12)
+
+
+def test_lepe_delta_kernel_is_identity():
+    v = rand_map(1, 5, 6, 4)
+    w = np.zeros((4, 5, 5))
+    w[:, 2, 2] = 1.0
+    np.testing.assert_array_equal(oracle.lepe(v, w, None), v)
+
+
+def test_attend_is_attention_plus_lepe():
+    wl = bra_synth.WORKLOADS["tiny_f32"]
+    x = bra_synth.make_inputs(wl)
+    idx, _ = oracle.route(x.q, x.k, wl.S, wl.topk)
+    total = oracle.attend(x.q, x.k, x.v, idx, wl.heads, wl.S, x.lepe_w, x.lepe_b)
+    parts = (oracle.routed_attention(x.q, x.k, x.v, idx, wl.heads, wl.S)
+             + oracle.lepe(x.v, x.lepe_w, x.lepe_b))
+    np.testing.assert_allclose(total, parts, atol=1e-14)
+    out, idx2 = oracle.forward(x.q, x.k, x.v, wl.heads, wl.S, wl.topk, x.lepe_w, x.lepe_b,
+                               threads=3)
+    np.testing.assert_array_equal(idx, idx2)
+    np.testing.assert_allclose(out, total, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# Worked example derived by hand
+# --------------------------------------------------------------------------
+
+def test_hand_worked_example():
+    """2x2 map, S = 2 (one token per region), C = 2, one head, top-2, 1x1 LePE.
+
+    Region r is token (r // 2, r % 2). Affinity rows (q_i . k_j):
+      q0=(1,0): [1, 0,-1, 0] -> [0, 1]  (tie 0 between j=1 and j=3 -> 1)
+      q1=(0,1): [0, 2, 0, 0] -> [1, 0]
+      q2=(1,1): [1, 2,-1, 0] -> [1, 0]
+      q3=(2,0): [2, 0,-2, 0] -> [0, 1]
+    With s = 1/sqrt(2) and sig(z) = 1/(1+e^-z), the softmax over the two
+    routed keys gives out0 = (sig(s), 1-sig(s)), out1 = (1-sig(2s), sig(2s)),
+    out2 = (1-sig(s), sig(s)), out3 = (sig(2s), 1-sig(2s)). Region 2's value
+    (2, 2) is routed by nobody and must not appear. LePE with w = (0.5, -2),
+    bias = (0.25, 1) adds (0.5 v0 + 0.25, -2 v1 + 1) per token.
+    """
+    q = np.array([[1, 0], [0, 1], [1, 1], [2, 0]], float).reshape(1, 2, 2, 2)
+    k = np.array([[1, 0], [0, 2], [-1, 0], [0, 0]], float).reshape(1, 2, 2, 2)
+    v = np.array([[1, 0], [0, 1], [2, 2], [0, -1]], float).reshape(1, 2, 2, 2)
+    w = np.array([0.5, -2.0]).reshape(2, 1, 1)
+    bias = np.array([0.25, 1.0])
+    out, idx = oracle.forward(q, k, v, 1, 2, 2, w, bias)
+    np.testing.assert_array_equal(idx[0], [[0, 1], [1, 0], [1, 0], [0, 1]])
+    sig = lambda z: 1.0 / (1.0 + math.exp(-z))
+    s = 1.0 / math.sqrt(2.0)
+    attn = np.array([[sig(s), 1 - sig(s)], [1 - sig(2 * s), sig(2 * s)],
+                     [1 - sig(s), sig(s)], [sig(2 * s), 1 - sig(2 * s)]])
+    vv = v.reshape(4, 2)
+    lepe = np.stack([0.5 * vv[:, 0] + 0.25, -2.0 * vv[:, 1] + 1.0], axis=1)
+    np.testing.assert_allclose(out.reshape(4, 2), attn + lepe, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# Facts the pages print
+# --------------------------------------------------------------------------
+
+def test_shapes_match_page_annotations():
+    with open(os.path.join(GOLDEN, "p1_shape_annotations.json")) as f:
+        g = json.load(f)
+    e = g["example"]
+    H, W, C, S, k = e["H"], e["W"], e["C"], e["S"], e["topk"]
+    env = {"S^2": S * S, "HW/S^2": H * W // (S * S), "C": C, "k": k,
+           "k*HW/S^2": k * H * W // (S * S)}
+    shp = {n: tuple(env[s] for s in dims) for n, dims in g["shapes"].items()}
+    x = np.ones((1, H, W, C))
+    assert region_tokens_per_page(H, W, S).shape == shp["partitioned_tokens"][:2]
+    assert oracle.region_means(x, S)[0].shape == shp["region_query_mean"]
+    idx, A = oracle.route(x, x, S, k)
+    assert A[0].shape == shp["region_affinity"]
+    assert idx[0].shape == shp["routing_index"]
+    p, _, _ = oracle.query_probs(x, x, x, idx, 2, S, 0, 0, 0, 0)
+    assert p.shape == (shp["gathered_keys"][1],)
+
+
+def test_workloads_follow_page_stage_settings():
+    with open(os.path.join(GOLDEN, "p1_stage_routing.json")) as f:
+        g = json.load(f)
+    W = bra_synth.WORKLOADS
+    # ImageNet-224 stage maps: stride 4 -> 56, 8 -> 28, 16 -> 14
+    for name, stage in [("stage1_bf16", "stage1"), ("stage2_bf16", "stage2"),
+                        ("stage3_bf16", "stage3")]:
+        assert W[name].topk == g["stage_topk"][stage]
+        assert W[name].H == 224 // g["stage_stride"][stage]
+        assert W[name].S == g["region_grid_S"]["classification"]
+    assert W["seg512_bf16"].S == g["region_grid_S"]["segmentation"]
+    assert W["seg512_bf16"].H == 512 // g["stage_stride"]["stage1"]
+
+
+def test_oracle_rejects_bad_arguments():
+    x = np.ones((1, 6, 6, 4))
+    with pytest.raises(ValueError):
+        oracle.region_means(x, 4)  # 6 % 4 != 0
+    with pytest.raises(ValueError):
+        oracle.route(x, x, 3, 10)  # topk > S^2
+    with pytest.raises(ValueError):
+        oracle.lepe(x, np.ones((4, 2, 2)), None)  # even kernel
