@@ -1,0 +1,133 @@
+/*
+ * bra.h -- C ABI of the Bi-Level Routing Attention (BRA) forward for B300
+ * (sm_103a). BRA is the attention of BiFormer.
+ *
+ * Sources of the operations (web pages about BiFormer):
+ *   "CVPR2023：BiFormer中的双层路由注意力机制解析" (cybasar.com), §2-§3:
+ *       region partition, region-mean Q/K, region affinity, top-k routing,
+ *       gather of the routed K/V, softmax attention, out += lce(v).
+ *   "从静态到动态：BRA双层路由注意力如何革新视觉Transformer的计算范式"
+ *       (snabindia.com), §2 (mean pooling per region), §4 (TopkRouting,
+ *       LePE as a depthwise nn.Conv2d with padding ks//2, groups = dim).
+ *   "BiFormer: Vision Transformer mit Bi-Level-Routing-Attention"
+ *       (hyper.ai abstract of arXiv 2303.08810): token-to-token attention
+ *       over the union of the routed regions.
+ *
+ * Conventions shared by every entry point
+ *   Layout     q, k, v and out are contiguous channels-last [B, H, W, C]
+ *              arrays in DEVICE memory, of type float32 (BRA_F32) or bfloat16
+ *              (BRA_BF16); out has the type of q. Regions are the S x S grid
+ *              numbered row-major; region r covers rows (r / S) * H/S ... and
+ *              columns (r % S) * W/S ... . Head h owns channels
+ *              [h * d, (h + 1) * d), d = C / heads.
+ *   LePE       lepe_w is float32 [C, ks, ks] (device), lepe_b float32 [C]
+ *              (device) or NULL for no bias. Zero padding at the image border.
+ *   Routing    idx is int32 [B, S*S, topk] (device): for each query region the
+ *              topk regions of largest affinity, largest first, ties to the
+ *              lowest region index. The affinity is mean(q_r) . mean(k_r)
+ *              over all C channels, computed in float32.
+ *   Ownership  The caller allocates and owns every buffer. No entry point
+ *              allocates, frees or synchronises: all work is enqueued on
+ *              `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *   Errors     Arguments are checked before anything is enqueued; on a
+ *              non-zero return nothing was launched. A launch failure returns
+ *              BRA_ERR_CUDA. Faults that happen on the device surface at the
+ *              caller's next synchronisation. Device-side checks (a wait that
+ *              gave up, a routing index out of range) set a status word read
+ *              by bra_device_status(). Nothing throws across the ABI.
+ *   Aliasing   out must not overlap q, k or v.
+ *   Threads    The library keeps no per-call state; calls on different
+ *              streams may run concurrently.
+ *   Empty      B == 0 is valid and enqueues nothing.
+ */
+#ifndef BRA_H_
+#define BRA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum bra_status {
+  BRA_OK = 0,
+  BRA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, aliasing */
+  BRA_ERR_UNSUPPORTED = 2, /* valid BRA, but a shape this build does not run */
+  BRA_ERR_CUDA = 3,        /* a CUDA call or launch failed */
+  BRA_ERR_TIMEOUT = 4      /* a device-side wait gave up (bra_device_status) */
+};
+
+enum bra_dtype { BRA_F32 = 0, BRA_BF16 = 1 };
+
+/*
+ * bra_route -- region-level routing (steps "q_r = q.mean", "A_r = q_r k_r^T",
+ * "I_r = topk(A_r)" of the cybasar page §3; TopkRouting of the snabindia page
+ * §4).
+ *   q, k      [B, H, W, C] device, dtype
+ *   B..C, S   map size and region grid; H and W must be multiples of S
+ *   topk      1 <= topk <= S*S
+ *   idx       out: int32 [B, S*S, topk] device
+ *   affinity  out (optional, may be NULL): float32 [B, S*S, S*S] device, the
+ *             unscaled region affinity the selection was taken on
+ * Supported: S*S <= 1024, B <= 65535, C % 8 == 0 (bf16) or C % 4 == 0
+ * (f32), and 2 * ceil(S*S / 8) * C * 4 bytes of region means per CTA within
+ * 200 KB; otherwise BRA_ERR_UNSUPPORTED.
+ */
+int bra_route(const void *q, const void *k, int B, int H, int W, int C, int S,
+              int topk, int dtype, int32_t *idx, float *affinity, void *stream);
+
+/*
+ * bra_attend -- token-to-token attention over the routed regions plus LePE
+ * (steps "k_g = gather(k, I_r)", "attn = softmax(q k_g^T * scale)",
+ * "out = attn v_g", "out += lce(v)" of the cybasar page §3; the LePE conv of
+ * the snabindia page §4). The gathered K/V are never written to memory.
+ *   q, k, v   [B, H, W, C] device, dtype
+ *   idx       int32 [B, S*S, topk] device, values in [0, S*S) (an index out of
+ *             range reads zeros and sets the device status word)
+ *   heads     C % heads == 0; scale is (C/heads)^-1/2
+ *   lepe_w/b  see above; lepe_ks odd, 1..7
+ *   out       [B, H, W, C] device, dtype of q
+ * Supported: bf16 with C % 64 == 0 and d == 32; f32 with C % 4 == 0 and
+ * d <= 64; shared-memory footprint within the per-block limit. Otherwise
+ * BRA_ERR_UNSUPPORTED.
+ */
+int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
+               int B, int H, int W, int C, int heads, int S, int topk,
+               const float *lepe_w, const float *lepe_b, int lepe_ks, int dtype,
+               void *out, void *stream);
+
+/*
+ * bra_forward -- bra_route then bra_attend on one stream.
+ *   idx_workspace  device buffer of bra_idx_workspace_bytes(B, S, topk)
+ *                  bytes; receives the routing index.
+ * Other arguments as above.
+ */
+int bra_forward(const void *q, const void *k, const void *v, int B, int H,
+                int W, int C, int heads, int S, int topk, const float *lepe_w,
+                const float *lepe_b, int lepe_ks, int dtype,
+                int32_t *idx_workspace, void *out, void *stream);
+
+/* Bytes of the routing index [B, S*S, topk] int32; 0 on invalid sizes. */
+size_t bra_idx_workspace_bytes(int B, int S, int topk);
+
+/*
+ * bra_device_status -- synchronise `stream`, then read the device status word
+ * that kernels set on the current device. Returns BRA_OK, BRA_ERR_TIMEOUT (a
+ * bounded wait gave up), BRA_ERR_INVALID_ARG (a routing index was out of
+ * range) or BRA_ERR_CUDA (the synchronisation itself failed). With clear != 0
+ * the word is reset to zero afterwards.
+ */
+int bra_device_status(void *stream, int clear);
+
+/* Static text for a status code. */
+const char *bra_status_string(int status);
+
+/* Version of this ABI (major * 100 + minor). */
+int bra_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BRA_H_ */

@@ -1,0 +1,120 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Small shapes span several tiles, ragged regions (slots padded to 8 rows),
+LePE borders, one region (dense attention), all regions routed and large
+region grids; the full-size workloads run at the sizes the benchmark times,
+with every output compared against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bra_synth
+import oracle
+import vision_transformer_sparse_route_b300 as bra
+from bra_synth import Workload
+from parity import TOL, device_inputs, run_and_compare
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    Workload("n64_bf16", 3, 16, 16, 64, 2, 2, 2, 5, "bf16"),
+    Workload("ragged_n15_bf16", 2, 12, 20, 128, 4, 4, 3, 5, "bf16"),
+    Workload("n4_bf16", 2, 14, 14, 256, 8, 7, 16, 5, "bf16"),
+    Workload("one_region_bf16", 2, 8, 8, 64, 2, 1, 1, 5, "bf16"),
+    Workload("all_routed_bf16", 1, 16, 16, 64, 2, 2, 4, 3, "bf16"),
+    Workload("ks7_bf16", 2, 16, 16, 64, 2, 4, 2, 7, "bf16"),
+    Workload("ks1_bf16", 2, 16, 16, 64, 2, 4, 2, 1, "bf16"),
+    Workload("wide_region_bf16", 1, 4, 64, 64, 2, 2, 1, 5, "bf16"),
+    Workload("tall_region_bf16", 1, 40, 8, 64, 2, 4, 3, 5, "bf16"),
+    Workload("grid32_bf16", 1, 64, 64, 64, 2, 32, 2, 5, "bf16"),
+    Workload("n16_c128_bf16", 3, 28, 28, 128, 4, 7, 4, 5, "bf16"),
+    Workload("small_f32", 2, 12, 12, 64, 2, 3, 3, 5, "f32"),
+    Workload("ragged_f32", 1, 15, 10, 32, 1, 5, 4, 3, "f32"),
+    Workload("d64_f32", 1, 8, 8, 128, 2, 2, 2, 5, "f32"),
+    Workload("one_region_f32", 1, 6, 6, 64, 2, 1, 1, 5, "f32"),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_small_shapes_match_oracle(wl, cuda_device):
+    res = run_and_compare(wl, cuda_device, seed=7)
+    assert res["rows_set"] + res["rows_near_tie"] == res["rows"]
+
+
+@pytest.mark.parametrize("name", list(bra_synth.WORKLOADS))
+def test_full_workloads_match_oracle(name, cuda_device):
+    wl = bra_synth.WORKLOADS[name]
+    res = run_and_compare(wl, cuda_device, seed=0)
+    print(name, res)
+    # with these value distributions near-ties are rare
+    assert res["rows_near_tie"] <= max(2, res["rows"] // 1000)
+
+
+def test_attend_with_oracle_routing(cuda_device):
+    """bra_attend on the oracle's own routing (decoupled from bra_route)."""
+    wl = bra_synth.WORKLOADS["stage2_bf16"].replace(B=4)
+    x = bra_synth.make_inputs(wl, seed=3)
+    q, k, v, w, b = device_inputs(wl, x, cuda_device)
+    idx_o, _ = oracle.route(x.q, x.k, wl.S, wl.topk)
+    out = bra.attend(q, k, v, torch.from_numpy(idx_o).to(cuda_device), wl.heads, wl.S, w, b)
+    ref = oracle.attend(x.q, x.k, x.v, idx_o, wl.heads, wl.S, x.lepe_w, x.lepe_b)
+    err = np.abs(out.float().cpu().numpy() - ref).max()
+    assert err <= TOL["bf16"]
+
+
+def test_no_bias_and_repeated_routing(cuda_device):
+    """lepe_b = NULL; an index list that repeats a region counts its keys twice."""
+    wl = Workload("rep", 1, 16, 16, 64, 2, 2, 3, 5, "bf16")
+    x = bra_synth.make_inputs(wl, seed=5)
+    q, k, v, w, _ = device_inputs(wl, x, cuda_device)
+    idx = np.array([[[0, 0, 1], [1, 2, 1], [3, 3, 3], [2, 0, 1]]], dtype=np.int32)
+    out = bra.attend(q, k, v, torch.from_numpy(idx).to(cuda_device), wl.heads, wl.S, w, None)
+    ref = oracle.attend(x.q, x.k, x.v, idx, wl.heads, wl.S, x.lepe_w, None)
+    assert np.abs(out.float().cpu().numpy() - ref).max() <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_out_of_range_index_reads_zeros_and_flags(dtype, cuda_device):
+    wl = Workload("bad", 1, 16, 16, 64, 2, 2, 2, 3, dtype)
+    x = bra_synth.make_inputs(wl, seed=2)
+    q, k, v, w, b = device_inputs(wl, x, cuda_device)
+    idx = np.array([[[0, 1], [1, 9], [2, -1], [3, 0]]], dtype=np.int32)
+    bra.device_status(clear=True)
+    out = bra.attend(q, k, v, torch.from_numpy(idx).to(cuda_device), wl.heads, wl.S, w, b)
+    assert bra.device_status(clear=True) == bra.BRA_ERR_INVALID_ARG
+    assert bra.device_status(clear=True) == bra.BRA_OK
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    # rows whose routing is valid are unaffected
+    good = np.array([[[0, 1], [1, 0], [2, 0], [3, 0]]], dtype=np.int32)
+    ref = oracle.attend(x.q, x.k, x.v, good, wl.heads, wl.S, x.lepe_w, x.lepe_b)
+    assert np.abs(got[:, :8, :8] - ref[:, :8, :8]).max() <= TOL[dtype]
+
+
+def test_empty_batch_is_a_no_op(cuda_device):
+    q = torch.empty((0, 14, 14, 64), dtype=torch.bfloat16, device=cuda_device)
+    w = torch.zeros((64, 5, 5), device=cuda_device)
+    out, idx = bra.forward(q, q.clone(), q.clone(), 2, 7, 4, w, None)
+    assert out.shape == q.shape and idx.shape == (0, 49, 4)
+
+
+def test_unsupported_shape_raises(cuda_device):
+    q = torch.zeros((1, 8, 8, 64), dtype=torch.bfloat16, device=cuda_device)
+    w = torch.zeros((64, 5, 5), device=cuda_device)
+    with pytest.raises(bra.BraError) as e:
+        bra.forward(q, q.clone(), q.clone(), 1, 2, 1, w, None)  # d = 64 in bf16
+    assert e.value.status == bra.BRA_ERR_UNSUPPORTED
+
+
+def test_side_stream_and_determinism(cuda_device):
+    wl = bra_synth.WORKLOADS["stage3_bf16"].replace(B=2)
+    x = bra_synth.make_inputs(wl, seed=11)
+    q, k, v, w, b = device_inputs(wl, x, cuda_device)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, i1 = bra.forward(q, k, v, wl.heads, wl.S, wl.topk, w, b, stream=s)
+    s.synchronize()
+    o2, i2 = bra.forward(q, k, v, wl.heads, wl.S, wl.topk, w, b)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(o1, o2)

@@ -1,0 +1,175 @@
+"""Bi-Level Routing Attention (BRA) forward on B300 (sm_103a).
+
+Python binding of the C ABI declared in include/bra.h. It only marshals
+arguments: every step of the computation runs in the CUDA kernels of
+libbra.so, and importing fails loudly when that library has not been built
+(`python -m vision_transformer_sparse_route_b300.build`). Tensors are torch
+tensors (torch supplies device memory and streams), contiguous, channels-last
+[B, H, W, C], float32 or bfloat16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["BraError", "route", "attend", "forward", "forward_host",
+           "idx_workspace_bytes", "device_status", "library_path", "SYMBOLS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libbra.so")
+
+BRA_OK, BRA_ERR_INVALID_ARG, BRA_ERR_UNSUPPORTED, BRA_ERR_CUDA, BRA_ERR_TIMEOUT = range(5)
+BRA_F32, BRA_BF16 = 0, 1
+
+# Entry points of include/bra.h with their ctypes signatures.
+_P, _I = ctypes.c_void_p, ctypes.c_int
+SYMBOLS = {
+    "bra_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "bra_attend": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
+    "bra_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
+    "bra_idx_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "bra_device_status": (_I, [_P, _I]),
+    "bra_status_string": (ctypes.c_char_p, [_I]),
+    "bra_abi_version": (_I, []),
+}
+
+_lib = None
+
+
+class BraError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m vision_transformer_sparse_route_b300.build`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SYMBOLS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _load().bra_status_string(status).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return BRA_F32
+    if t.dtype == torch.bfloat16:
+        return BRA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != BRA_OK:
+        raise BraError(rc, what)
+
+
+def _map(t: torch.Tensor, name: str):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, W, C]")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.shape
+
+
+def idx_workspace_bytes(B: int, S: int, topk: int) -> int:
+    return _load().bra_idx_workspace_bytes(B, S, topk)
+
+
+def route(q, k, S: int, topk: int, idx=None, affinity=None, stream=None):
+    """Top-k region routing; returns idx int32 [B, S*S, topk] (and fills
+    `affinity` float32 [B, S*S, S*S] when given)."""
+    B, H, W, C = _map(q, "q")
+    _map(k, "k")
+    if idx is None:
+        idx = torch.empty((B, S * S, topk), dtype=torch.int32, device=q.device)
+    rc = _load().bra_route(_ptr(q), _ptr(k), B, H, W, C, S, topk, _dtype_code(q),
+                           _ptr(idx), _ptr(affinity), _stream(stream))
+    _check(rc, "bra_route")
+    return idx
+
+
+def attend(q, k, v, idx, heads: int, S: int, lepe_w, lepe_b=None, out=None, stream=None):
+    """Routed attention + LePE given the routing index; returns out."""
+    B, H, W, C = _map(q, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    topk = idx.shape[-1]
+    rc = _load().bra_attend(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), B, H, W, C, heads, S,
+                            topk, _ptr(lepe_w), _ptr(lepe_b), lepe_w.shape[-1],
+                            _dtype_code(q), _ptr(out), _stream(stream))
+    _check(rc, "bra_attend")
+    return out
+
+
+def forward(q, k, v, heads: int, S: int, topk: int, lepe_w, lepe_b=None, out=None,
+            idx=None, stream=None):
+    """The whole BRA forward on device tensors; returns (out, idx)."""
+    B, H, W, C = _map(q, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    if idx is None:
+        idx = torch.empty((B, S * S, topk), dtype=torch.int32, device=q.device)
+    rc = _load().bra_forward(_ptr(q), _ptr(k), _ptr(v), B, H, W, C, heads, S, topk,
+                             _ptr(lepe_w), _ptr(lepe_b), lepe_w.shape[-1], _dtype_code(q),
+                             _ptr(idx), _ptr(out), _stream(stream))
+    _check(rc, "bra_forward")
+    return out, idx
+
+
+class HostBuffers:
+    """Device staging buffers for forward_host, reused across calls."""
+
+    def __init__(self, shape, dtype, S: int, topk: int, device):
+        self.q, self.k, self.v, self.out = (torch.empty(shape, dtype=dtype, device=device)
+                                            for _ in range(4))
+        self.idx = torch.empty((shape[0], S * S, topk), dtype=torch.int32, device=device)
+
+
+def forward_host(q, k, v, heads: int, S: int, topk: int, lepe_w, lepe_b, out,
+                 buffers: HostBuffers, stream=None):
+    """BRA forward on host tensors (pinned for asynchronous copies): copies
+    q, k, v to the device buffers, runs bra_forward and copies out back, all
+    on `stream`. lepe_w / lepe_b are device tensors."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    with torch.cuda.stream(s):
+        buffers.q.copy_(q, non_blocking=True)
+        buffers.k.copy_(k, non_blocking=True)
+        buffers.v.copy_(v, non_blocking=True)
+        forward(buffers.q, buffers.k, buffers.v, heads, S, topk, lepe_w, lepe_b,
+                out=buffers.out, idx=buffers.idx, stream=s)
+        out.copy_(buffers.out, non_blocking=True)
+    return out
+
+
+def device_status(stream=None, clear: bool = True) -> int:
+    """Synchronises the stream and returns the device status word as a
+    status code (see include/bra.h)."""
+    return _load().bra_device_status(_stream(stream), 1 if clear else 0)

@@ -1,0 +1,403 @@
+// bra.cu -- the C ABI of include/bra.h: argument checks, TMA tensor maps and
+// kernel launches for the Bi-Level Routing Attention forward on sm_103a.
+// All kernels live in this one translation unit so that they share the
+// device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "bra.h"
+#include "attend_bf16.cuh"
+#include "attend_f32.cuh"
+#include "route.cuh"
+
+namespace {
+
+using bra::AttendF32Geom;
+using bra::AttendGeom;
+
+constexpr size_t kMaxSmemPerBlock = 227 * 1024;
+constexpr size_t kRouteSmemLimit = 200 * 1024;
+
+inline int elem_size(int dtype) { return dtype == BRA_F32 ? 4 : 2; }
+
+inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a);
+  const uintptr_t y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+inline size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+// Checks shared by every entry point. Returns BRA_OK or an error code.
+int check_map_args(int B, int H, int W, int C, int S, int topk, int dtype) {
+  if (B < 0 || H <= 0 || W <= 0 || C <= 0 || S <= 0 || topk <= 0)
+    return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_F32 && dtype != BRA_BF16) return BRA_ERR_INVALID_ARG;
+  if (H % S || W % S) return BRA_ERR_INVALID_ARG;
+  if ((long long)S * S < topk) return BRA_ERR_INVALID_ARG;
+  if ((long long)B * H * W * C > (1ll << 40)) return BRA_ERR_UNSUPPORTED;
+  return BRA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? BRA_OK : BRA_ERR_CUDA; }
+
+// ------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 [B, H, W, C] map; box = 64 channels x box_w x box_h x 1 image,
+// 128-byte swizzle, zero fill outside the map.
+bool make_map(CUtensorMap *m, const void *base, int B, int H, int W, int C,
+              int box_w, int box_h) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2,
+                           (cuuint64_t)H * W * C * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_w, (cuuint32_t)box_h, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Raises a kernel's dynamic shared-memory limit to the per-block maximum,
+// once per kernel and process.
+cudaError_t allow_smem(const void *kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::vector<const void *> done;
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(mu);
+  if (std::find(done.begin(), done.end(), kernel) != done.end()) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(
+      kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmemPerBlock);
+  if (e == cudaSuccess) done.push_back(kernel);
+  return e;
+}
+
+// ------------------------------------------------------------------ route
+// Whether the route kernel can keep all K means in local shared memory.
+bool route_local_k(int R, int C) {
+  const int CL = std::min(bra::kRouteMaxCluster, R);
+  return bra::RouteSmem::floats(R, C, CL, true) * sizeof(float) <= kRouteSmemLimit;
+}
+
+template <typename T, int MAXJ, bool LOCAL_K>
+int launch_route_k(const void *q, const void *k, int B, int H, int W, int C,
+                   int S, int topk, int32_t *idx, float *aff, cudaStream_t s) {
+  const int R = S * S;
+  const int CL = std::min(bra::kRouteMaxCluster, R);
+  const size_t smem = bra::RouteSmem::floats(R, C, CL, LOCAL_K) * sizeof(float);
+  auto kern = bra::bra_route_kernel<T, MAXJ, LOCAL_K>;
+  cudaError_t e = allow_smem(reinterpret_cast<const void *>(kern), smem);
+  if (e != cudaSuccess) return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL, B, 1);
+  cfg.blockDim = dim3(bra::kRouteThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T *>(q),
+                         static_cast<const T *>(k), H, W, C, S, topk, idx, aff);
+  return cuda_status(e);
+}
+
+template <typename T, int MAXJ>
+int launch_route_t(const void *q, const void *k, int B, int H, int W, int C,
+                   int S, int topk, int32_t *idx, float *aff, cudaStream_t s) {
+  if (route_local_k(S * S, C))
+    return launch_route_k<T, MAXJ, true>(q, k, B, H, W, C, S, topk, idx, aff, s);
+  return launch_route_k<T, MAXJ, false>(q, k, B, H, W, C, S, topk, idx, aff, s);
+}
+
+template <typename T>
+int launch_route_dtype(const void *q, const void *k, int B, int H, int W, int C,
+                       int S, int topk, int32_t *idx, float *aff, cudaStream_t s) {
+  const int R = S * S;
+  if (R <= 32) return launch_route_t<T, 1>(q, k, B, H, W, C, S, topk, idx, aff, s);
+  if (R <= 64) return launch_route_t<T, 2>(q, k, B, H, W, C, S, topk, idx, aff, s);
+  if (R <= 128) return launch_route_t<T, 4>(q, k, B, H, W, C, S, topk, idx, aff, s);
+  if (R <= 256) return launch_route_t<T, 8>(q, k, B, H, W, C, S, topk, idx, aff, s);
+  if (R <= 512) return launch_route_t<T, 16>(q, k, B, H, W, C, S, topk, idx, aff, s);
+  return launch_route_t<T, 32>(q, k, B, H, W, C, S, topk, idx, aff, s);
+}
+
+int check_route(const void *q, const void *k, int B, int H, int W, int C, int S,
+                int topk, int dtype, const int32_t *idx) {
+  int rc = check_map_args(B, H, W, C, S, topk, dtype);
+  if (rc) return rc;
+  if (B == 0) return BRA_OK;
+  if (!q || !k || !idx) return BRA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k)) return BRA_ERR_INVALID_ARG;
+  const int R = S * S;
+  if (R > 1024 || B > 65535) return BRA_ERR_UNSUPPORTED;
+  if (C % (dtype == BRA_F32 ? 4 : 8)) return BRA_ERR_UNSUPPORTED;
+  const int CL = std::min(bra::kRouteMaxCluster, R);
+  if (bra::RouteSmem::floats(R, C, CL, false) * sizeof(float) > kRouteSmemLimit)
+    return BRA_ERR_UNSUPPORTED;
+  return BRA_OK;
+}
+
+int launch_route(const void *q, const void *k, int B, int H, int W, int C, int S,
+                 int topk, int dtype, int32_t *idx, float *aff, cudaStream_t s) {
+  if (dtype == BRA_F32)
+    return launch_route_dtype<float>(q, k, B, H, W, C, S, topk, idx, aff, s);
+  return launch_route_dtype<__nv_bfloat16>(q, k, B, H, W, C, S, topk, idx, aff, s);
+}
+
+// ----------------------------------------------------------------- attend
+bool lepe_ks_supported(int ks) { return ks == 1 || ks == 3 || ks == 5 || ks == 7; }
+
+bool plan_attend_bf16(int H, int W, int C, int heads, int S, int topk, int ks,
+                      AttendGeom *g, size_t *smem) {
+  if (C % 64 || C / heads != 32) return false;
+  AttendGeom a = {};
+  a.H = H; a.W = W; a.C = C; a.S = S; a.heads = heads; a.topk = topk;
+  a.hr = H / S; a.wr = W / S; a.n = a.hr * a.wr; a.R = S * S;
+  if (a.hr > 256 || a.wr + ks - 1 > 256 || a.hr + ks - 1 > 256) return false;
+  a.nc = C / 64;
+  a.slot = (int)round_up(a.n, 8);
+  a.kv_rows = (int)round_up((size_t)topk * a.slot, 64);
+  a.q_blocks = (a.n + 15) / 16;
+  a.halo_w = a.wr + ks - 1;
+  a.halo_h = a.hr + ks - 1;
+  a.q_chunk = (uint32_t)round_up((size_t)a.q_blocks * 16 * 128, 1024);
+  a.kv_chunk = (uint32_t)a.kv_rows * 128u;
+  a.h_chunk = (uint32_t)round_up((size_t)a.halo_w * a.halo_h * 128, 1024);
+  a.o_stride = C + 8;
+  size_t off = (size_t)a.nc * a.q_chunk;
+  a.off_k = (uint32_t)off; off += (size_t)a.nc * a.kv_chunk;
+  a.off_v = (uint32_t)off; off += (size_t)a.nc * a.kv_chunk;
+  a.off_h = (uint32_t)off; off += (size_t)a.nc * a.h_chunk;
+  a.off_o = (uint32_t)off; off += round_up((size_t)a.n * a.o_stride * 4, 16);
+  a.off_bar = (uint32_t)off; off += 16;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
+  *smem = off + 1024;  // slack to align the base to 1024 bytes
+  *g = a;
+  return *smem <= kMaxSmemPerBlock;
+}
+
+bool plan_attend_f32(int H, int W, int C, int heads, int S, int topk, int ks,
+                     AttendF32Geom *g, size_t *smem) {
+  if (C % 4 || C / heads > 64) return false;
+  AttendF32Geom a = {};
+  a.H = H; a.W = W; a.C = C; a.S = S; a.heads = heads; a.topk = topk;
+  a.hr = H / S; a.wr = W / S; a.n = a.hr * a.wr; a.R = S * S;
+  a.halo_w = a.wr + ks - 1;
+  a.halo_h = a.hr + ks - 1;
+  a.nk = topk * a.n;
+  a.scale = (float)(1.0 / std::sqrt((double)(C / heads)));
+  size_t off = (size_t)a.n * C;
+  a.off_k = (int)off; off += (size_t)a.nk * (C + 1);
+  off = round_up(off, 4);
+  a.off_v = (int)off; off += (size_t)a.nk * C;
+  a.off_h = (int)off; off += (size_t)a.halo_w * a.halo_h * C;
+  a.off_p = (int)off; off += (size_t)(bra::kAttendF32Threads / 32) * a.nk;
+  *smem = off * sizeof(float);
+  *g = a;
+  return *smem <= kMaxSmemPerBlock;
+}
+
+template <int KS>
+int launch_attend_bf16_ks(const void *q, const void *k, const void *v,
+                          const int32_t *idx, int B, const float *w,
+                          const float *bias, void *out, const AttendGeom &g,
+                          size_t smem, cudaStream_t s) {
+  CUtensorMap tq, tk, tv, th, to;
+  if (!make_map(&tq, q, B, g.H, g.W, g.C, g.wr, g.hr) ||
+      !make_map(&tk, k, B, g.H, g.W, g.C, g.wr, g.hr) ||
+      !make_map(&tv, v, B, g.H, g.W, g.C, g.wr, g.hr) ||
+      !make_map(&th, v, B, g.H, g.W, g.C, g.halo_w, g.halo_h) ||
+      !make_map(&to, out, B, g.H, g.W, g.C, g.wr, g.hr))
+    return BRA_ERR_CUDA;
+  auto kern = bra::bra_attend_bf16_kernel<KS>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess) return BRA_ERR_CUDA;
+  const unsigned grid = (unsigned)((size_t)B * g.R);
+  kern<<<grid, bra::kAttendThreads, smem, s>>>(tq, tk, tv, th, to, idx, w, bias, g);
+  return cuda_status(cudaGetLastError());
+}
+
+template <int KS>
+int launch_attend_f32_ks(const void *q, const void *k, const void *v,
+                         const int32_t *idx, int B, const float *w,
+                         const float *bias, void *out, const AttendF32Geom &g,
+                         size_t smem, cudaStream_t s) {
+  auto kern = bra::bra_attend_f32_kernel<KS>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess) return BRA_ERR_CUDA;
+  const unsigned grid = (unsigned)((size_t)B * g.R);
+  kern<<<grid, bra::kAttendF32Threads, smem, s>>>(
+      static_cast<const float *>(q), static_cast<const float *>(k),
+      static_cast<const float *>(v), idx, w, bias, static_cast<float *>(out), g);
+  return cuda_status(cudaGetLastError());
+}
+
+int check_attend(const void *q, const void *k, const void *v, const int32_t *idx,
+                 int B, int H, int W, int C, int heads, int S, int topk,
+                 const float *w, int ks, int dtype, const void *out) {
+  int rc = check_map_args(B, H, W, C, S, topk, dtype);
+  if (rc) return rc;
+  if (heads <= 0 || C % heads) return BRA_ERR_INVALID_ARG;
+  if (ks <= 0 || ks % 2 == 0) return BRA_ERR_INVALID_ARG;
+  if (B == 0) return BRA_OK;
+  if (!q || !k || !v || !idx || !w || !out) return BRA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return BRA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)B * H * W * C * elem_size(dtype);
+  if (overlap(out, bytes, q, bytes) || overlap(out, bytes, k, bytes) ||
+      overlap(out, bytes, v, bytes))
+    return BRA_ERR_INVALID_ARG;
+  if (!lepe_ks_supported(ks)) return BRA_ERR_UNSUPPORTED;
+  if ((size_t)B * S * S > 0x7fffffffu) return BRA_ERR_UNSUPPORTED;
+  size_t smem;
+  if (dtype == BRA_BF16) {
+    AttendGeom g;
+    if (!plan_attend_bf16(H, W, C, heads, S, topk, ks, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+  } else {
+    AttendF32Geom g;
+    if (!plan_attend_f32(H, W, C, heads, S, topk, ks, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+  }
+  return BRA_OK;
+}
+
+int launch_attend(const void *q, const void *k, const void *v, const int32_t *idx,
+                  int B, int H, int W, int C, int heads, int S, int topk,
+                  const float *w, const float *bias, int ks, int dtype, void *out,
+                  cudaStream_t s) {
+  size_t smem;
+  if (dtype == BRA_BF16) {
+    AttendGeom g;
+    plan_attend_bf16(H, W, C, heads, S, topk, ks, &g, &smem);
+    switch (ks) {
+      case 1: return launch_attend_bf16_ks<1>(q, k, v, idx, B, w, bias, out, g, smem, s);
+      case 3: return launch_attend_bf16_ks<3>(q, k, v, idx, B, w, bias, out, g, smem, s);
+      case 5: return launch_attend_bf16_ks<5>(q, k, v, idx, B, w, bias, out, g, smem, s);
+      default: return launch_attend_bf16_ks<7>(q, k, v, idx, B, w, bias, out, g, smem, s);
+    }
+  }
+  AttendF32Geom g;
+  plan_attend_f32(H, W, C, heads, S, topk, ks, &g, &smem);
+  switch (ks) {
+    case 1: return launch_attend_f32_ks<1>(q, k, v, idx, B, w, bias, out, g, smem, s);
+    case 3: return launch_attend_f32_ks<3>(q, k, v, idx, B, w, bias, out, g, smem, s);
+    case 5: return launch_attend_f32_ks<5>(q, k, v, idx, B, w, bias, out, g, smem, s);
+    default: return launch_attend_f32_ks<7>(q, k, v, idx, B, w, bias, out, g, smem, s);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int bra_route(const void *q, const void *k, int B, int H, int W, int C, int S,
+              int topk, int dtype, int32_t *idx, float *affinity, void *stream) {
+  int rc = check_route(q, k, B, H, W, C, S, topk, dtype, idx);
+  if (rc || B == 0) return rc;
+  (void)cudaGetLastError();
+  return launch_route(q, k, B, H, W, C, S, topk, dtype, idx, affinity,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
+               int B, int H, int W, int C, int heads, int S, int topk,
+               const float *lepe_w, const float *lepe_b, int lepe_ks, int dtype,
+               void *out, void *stream) {
+  int rc = check_attend(q, k, v, idx, B, H, W, C, heads, S, topk, lepe_w, lepe_ks,
+                        dtype, out);
+  if (rc || B == 0) return rc;
+  (void)cudaGetLastError();
+  return launch_attend(q, k, v, idx, B, H, W, C, heads, S, topk, lepe_w, lepe_b,
+                       lepe_ks, dtype, out, static_cast<cudaStream_t>(stream));
+}
+
+int bra_forward(const void *q, const void *k, const void *v, int B, int H, int W,
+                int C, int heads, int S, int topk, const float *lepe_w,
+                const float *lepe_b, int lepe_ks, int dtype,
+                int32_t *idx_workspace, void *out, void *stream) {
+  int rc = check_route(q, k, B, H, W, C, S, topk, dtype, idx_workspace);
+  if (rc) return rc;
+  rc = check_attend(q, k, v, idx_workspace, B, H, W, C, heads, S, topk, lepe_w,
+                    lepe_ks, dtype, out);
+  if (rc || B == 0) return rc;
+  const size_t ib = bra_idx_workspace_bytes(B, S, topk);
+  const size_t bytes = (size_t)B * H * W * C * elem_size(dtype);
+  if (overlap(idx_workspace, ib, out, bytes) || overlap(idx_workspace, ib, q, bytes) ||
+      overlap(idx_workspace, ib, k, bytes) || overlap(idx_workspace, ib, v, bytes))
+    return BRA_ERR_INVALID_ARG;
+  (void)cudaGetLastError();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_route(q, k, B, H, W, C, S, topk, dtype, idx_workspace, nullptr, s);
+  if (rc) return rc;
+  return launch_attend(q, k, v, idx_workspace, B, H, W, C, heads, S, topk, lepe_w,
+                       lepe_b, lepe_ks, dtype, out, s);
+}
+
+size_t bra_idx_workspace_bytes(int B, int S, int topk) {
+  if (B < 0 || S <= 0 || topk <= 0) return 0;
+  return (size_t)B * S * S * topk * sizeof(int32_t);
+}
+
+int bra_device_status(void *stream, int clear) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BRA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, bra::g_status, sizeof(v)) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  if (clear) {
+    const unsigned z = 0;
+    if (cudaMemcpyToSymbol(bra::g_status, &z, sizeof(z)) != cudaSuccess)
+      return BRA_ERR_CUDA;
+  }
+  if (v & bra::kStatusTimeout) return BRA_ERR_TIMEOUT;
+  if (v & bra::kStatusBadIndex) return BRA_ERR_INVALID_ARG;
+  return BRA_OK;
+}
+
+const char *bra_status_string(int status) {
+  switch (status) {
+    case BRA_OK: return "ok";
+    case BRA_ERR_INVALID_ARG: return "invalid argument";
+    case BRA_ERR_UNSUPPORTED: return "unsupported shape";
+    case BRA_ERR_CUDA: return "CUDA error";
+    case BRA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int bra_abi_version(void) { return 100; }
+
+}  // extern "C"
