@@ -74,9 +74,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 [B, H, W, C] map; box = 64 channels x box_w x box_h x 1 image,
-// 128-byte swizzle, zero fill outside the map.
+// zero fill outside the map; 128-byte swizzle for tiles read by ldmatrix.
 bool make_map(CUtensorMap *m, const void *base, int B, int H, int W, int C,
-              int box_w, int box_h) {
+              int box_w, int box_h, bool swizzle) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)B};
@@ -86,7 +86,8 @@ bool make_map(CUtensorMap *m, const void *base, int B, int H, int W, int C,
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -183,7 +184,22 @@ int launch_route(const void *q, const void *k, int B, int H, int W, int C, int S
 // ----------------------------------------------------------------- attend
 bool lepe_ks_supported(int ks) { return ks == 1 || ks == 3 || ks == 5 || ks == 7; }
 
-bool plan_attend_bf16(int H, int W, int C, int heads, int S, int topk, int ks,
+int sm_count() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!counts[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+int lepe_row_block(int hr) { return hr >= 8 ? 8 : hr >= 4 ? 4 : hr >= 2 ? 2 : 1; }
+
+bool plan_attend_bf16(int B, int H, int W, int C, int heads, int S, int topk, int ks,
                       AttendGeom *g, size_t *smem) {
   if (C % 64 || C / heads != 32) return false;
   AttendGeom a = {};
@@ -196,17 +212,33 @@ bool plan_attend_bf16(int H, int W, int C, int heads, int S, int topk, int ks,
   a.q_blocks = (a.n + 15) / 16;
   a.halo_w = a.wr + ks - 1;
   a.halo_h = a.hr + ks - 1;
+  a.units = B * a.R;
+  a.masked = (a.slot != a.n) || ((topk * a.slot) % 64 != 0);
+  const int rb = lepe_row_block(a.hr);
+  a.lepe_items = (C / 2) * a.wr * ((a.hr + rb - 1) / rb);
   a.q_chunk = (uint32_t)round_up((size_t)a.q_blocks * 16 * 128, 1024);
   a.kv_chunk = (uint32_t)a.kv_rows * 128u;
-  a.h_chunk = (uint32_t)round_up((size_t)a.halo_w * a.halo_h * 128, 1024);
+  a.h_chunk = (uint32_t)a.halo_w * a.halo_h * 128u;
+  a.o_chunk = (uint32_t)a.n * 128u;
+  a.off_k = a.nc * a.q_chunk;
+  a.off_v = a.off_k + a.nc * a.kv_chunk;
+  a.off_h = a.off_v + a.nc * a.kv_chunk;
+  a.stage_bytes = (uint32_t)round_up((size_t)a.off_h + (size_t)a.nc * a.h_chunk, 1024);
+  a.tx_bytes = a.nc * (a.o_chunk * (1u + 2u * topk) + a.h_chunk);
   a.o_stride = C + 8;
-  size_t off = (size_t)a.nc * a.q_chunk;
-  a.off_k = (uint32_t)off; off += (size_t)a.nc * a.kv_chunk;
-  a.off_v = (uint32_t)off; off += (size_t)a.nc * a.kv_chunk;
-  a.off_h = (uint32_t)off; off += (size_t)a.nc * a.h_chunk;
-  a.off_o = (uint32_t)off; off += round_up((size_t)a.n * a.o_stride * 4, 16);
-  a.off_bar = (uint32_t)off; off += 16;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
+  const size_t fixed = round_up((size_t)2 * a.nc * a.o_chunk, 1024) +
+                       round_up((size_t)a.n * a.o_stride * 4, 16) +
+                       round_up((size_t)(ks * ks + 1) * C * 4, 16) +
+                       2 * bra::kMaxStages * 8;
+  const size_t budget = kMaxSmemPerBlock - 1024;
+  if (fixed + a.stage_bytes > budget) return false;
+  a.stages = (int)std::min<size_t>(bra::kMaxStages, (budget - fixed) / a.stage_bytes);
+  size_t off = (size_t)a.stages * a.stage_bytes;
+  a.off_out = (uint32_t)off; off += round_up((size_t)2 * a.nc * a.o_chunk, 1024);
+  a.off_o = (uint32_t)off; off += round_up((size_t)a.n * a.o_stride * 4, 16);
+  a.off_w = (uint32_t)off; off += round_up((size_t)(ks * ks + 1) * C * 4, 16);
+  a.off_bar = (uint32_t)off; off += 2 * bra::kMaxStages * 8;
   *smem = off + 1024;  // slack to align the base to 1024 bytes
   *g = a;
   return *smem <= kMaxSmemPerBlock;
@@ -233,23 +265,45 @@ bool plan_attend_f32(int H, int W, int C, int heads, int S, int topk, int ks,
   return *smem <= kMaxSmemPerBlock;
 }
 
+template <int KS, int RB>
+int launch_attend_bf16_kr(const void *q, const void *k, const void *v,
+                          const int32_t *idx, int B, const float *w,
+                          const float *bias, void *out, const AttendGeom &g,
+                          size_t smem, bool pdl, cudaStream_t s) {
+  CUtensorMap tq, tk, tv, th, to;
+  if (!make_map(&tq, q, B, g.H, g.W, g.C, g.wr, g.hr, true) ||
+      !make_map(&tk, k, B, g.H, g.W, g.C, g.wr, g.hr, true) ||
+      !make_map(&tv, v, B, g.H, g.W, g.C, g.wr, g.hr, true) ||
+      !make_map(&th, v, B, g.H, g.W, g.C, g.halo_w, g.halo_h, false) ||
+      !make_map(&to, out, B, g.H, g.W, g.C, g.wr, g.hr, false))
+    return BRA_ERR_CUDA;
+  auto kern = bra::bra_attend_bf16_kernel<KS, RB>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min(g.units, sm_count()), 1, 1);
+  cfg.blockDim = dim3(bra::kAttendThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, th, to, idx, w, bias, g));
+}
+
 template <int KS>
 int launch_attend_bf16_ks(const void *q, const void *k, const void *v,
                           const int32_t *idx, int B, const float *w,
                           const float *bias, void *out, const AttendGeom &g,
-                          size_t smem, cudaStream_t s) {
-  CUtensorMap tq, tk, tv, th, to;
-  if (!make_map(&tq, q, B, g.H, g.W, g.C, g.wr, g.hr) ||
-      !make_map(&tk, k, B, g.H, g.W, g.C, g.wr, g.hr) ||
-      !make_map(&tv, v, B, g.H, g.W, g.C, g.wr, g.hr) ||
-      !make_map(&th, v, B, g.H, g.W, g.C, g.halo_w, g.halo_h) ||
-      !make_map(&to, out, B, g.H, g.W, g.C, g.wr, g.hr))
-    return BRA_ERR_CUDA;
-  auto kern = bra::bra_attend_bf16_kernel<KS>;
-  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess) return BRA_ERR_CUDA;
-  const unsigned grid = (unsigned)((size_t)B * g.R);
-  kern<<<grid, bra::kAttendThreads, smem, s>>>(tq, tk, tv, th, to, idx, w, bias, g);
-  return cuda_status(cudaGetLastError());
+                          size_t smem, bool pdl, cudaStream_t s) {
+  switch (lepe_row_block(g.hr)) {
+    case 8: return launch_attend_bf16_kr<KS, 8>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+    case 4: return launch_attend_bf16_kr<KS, 4>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+    case 2: return launch_attend_bf16_kr<KS, 2>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+    default: return launch_attend_bf16_kr<KS, 1>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+  }
 }
 
 template <int KS>
@@ -286,7 +340,7 @@ int check_attend(const void *q, const void *k, const void *v, const int32_t *idx
   size_t smem;
   if (dtype == BRA_BF16) {
     AttendGeom g;
-    if (!plan_attend_bf16(H, W, C, heads, S, topk, ks, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+    if (!plan_attend_bf16(B, H, W, C, heads, S, topk, ks, &g, &smem)) return BRA_ERR_UNSUPPORTED;
   } else {
     AttendF32Geom g;
     if (!plan_attend_f32(H, W, C, heads, S, topk, ks, &g, &smem)) return BRA_ERR_UNSUPPORTED;
@@ -297,16 +351,16 @@ int check_attend(const void *q, const void *k, const void *v, const int32_t *idx
 int launch_attend(const void *q, const void *k, const void *v, const int32_t *idx,
                   int B, int H, int W, int C, int heads, int S, int topk,
                   const float *w, const float *bias, int ks, int dtype, void *out,
-                  cudaStream_t s) {
+                  bool pdl, cudaStream_t s) {
   size_t smem;
   if (dtype == BRA_BF16) {
     AttendGeom g;
-    plan_attend_bf16(H, W, C, heads, S, topk, ks, &g, &smem);
+    plan_attend_bf16(B, H, W, C, heads, S, topk, ks, &g, &smem);
     switch (ks) {
-      case 1: return launch_attend_bf16_ks<1>(q, k, v, idx, B, w, bias, out, g, smem, s);
-      case 3: return launch_attend_bf16_ks<3>(q, k, v, idx, B, w, bias, out, g, smem, s);
-      case 5: return launch_attend_bf16_ks<5>(q, k, v, idx, B, w, bias, out, g, smem, s);
-      default: return launch_attend_bf16_ks<7>(q, k, v, idx, B, w, bias, out, g, smem, s);
+      case 1: return launch_attend_bf16_ks<1>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+      case 3: return launch_attend_bf16_ks<3>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+      case 5: return launch_attend_bf16_ks<5>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+      default: return launch_attend_bf16_ks<7>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
     }
   }
   AttendF32Geom g;
@@ -341,7 +395,7 @@ int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
   if (rc || B == 0) return rc;
   (void)cudaGetLastError();
   return launch_attend(q, k, v, idx, B, H, W, C, heads, S, topk, lepe_w, lepe_b,
-                       lepe_ks, dtype, out, static_cast<cudaStream_t>(stream));
+                       lepe_ks, dtype, out, false, static_cast<cudaStream_t>(stream));
 }
 
 int bra_forward(const void *q, const void *k, const void *v, int B, int H, int W,
@@ -362,8 +416,10 @@ int bra_forward(const void *q, const void *k, const void *v, int B, int H, int W
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = launch_route(q, k, B, H, W, C, S, topk, dtype, idx_workspace, nullptr, s);
   if (rc) return rc;
+  // programmatic dependent launch: the attend grid may start while the route
+  // grid drains; it waits for that grid only where it reads the routing index
   return launch_attend(q, k, v, idx_workspace, B, H, W, C, heads, S, topk, lepe_w,
-                       lepe_b, lepe_ks, dtype, out, s);
+                       lepe_b, lepe_ks, dtype, out, true, s);
 }
 
 size_t bra_idx_workspace_bytes(int B, int S, int topk) {

@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(kRouteThreads)
     bra_route_kernel(const T *__restrict__ q, const T *__restrict__ k, int H,
                      int W, int C, int S, int topk, int32_t *__restrict__ idx,
                      float *__restrict__ affinity) {
+  // A dependent grid launched with programmatic serialization may start now;
+  // it waits for this grid before it reads the routing index.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
