@@ -43,7 +43,7 @@ CSRC = os.path.join(ROOT, "vision_transformer_sparse_route_b300", "csrc")
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="stage1_bf16", choices=list(bra_synth.WORKLOADS))
