@@ -108,6 +108,35 @@ int bra_forward(const void *q, const void *k, const void *v, int B, int H,
                 const float *lepe_b, int lepe_ks, int dtype,
                 int32_t *idx_workspace, void *out, void *stream);
 
+/*
+ * bra_forward_static -- bra_forward for callers that cannot allocate device
+ * memory. It has no counterpart on the pages: it exists for callers that are
+ * handed only their input and output buffers and may not call cudaMalloc,
+ * such as a plugin inside an inference engine that owns the whole device
+ * memory budget, or a latency-critical loop where cudaMalloc's implicit
+ * synchronisation is not acceptable. The routing index lives in a fixed
+ * array inside the library (BRA_STATIC_IDX_MAX_ENTRIES int32 = 1 MiB per
+ * GPU, held until the process exits) instead of a caller workspace; nothing
+ * is allocated, freed or synchronised.
+ *   Arguments    as bra_forward, without idx_workspace.
+ *   Limit        B * S*S * topk <= BRA_STATIC_IDX_MAX_ENTRIES, otherwise
+ *                BRA_ERR_UNSUPPORTED and nothing is launched.
+ *   First call   the first call on each device looks up the array's device
+ *                address (cudaGetSymbolAddress) with that device current;
+ *                make that first call before any stream capture.
+ *   Sharing      every call on a device uses the same array: calls that
+ *                overlap on the GPU (on different streams, or from several
+ *                threads) race on it. Serialise them, or use bra_forward
+ *                with a workspace per stream. Each call overwrites the index
+ *                it reads, so no clearing is needed between calls.
+ *   The index is not returned; use bra_route for it.
+ */
+#define BRA_STATIC_IDX_MAX_ENTRIES (1 << 18)
+int bra_forward_static(const void *q, const void *k, const void *v, int B,
+                       int H, int W, int C, int heads, int S, int topk,
+                       const float *lepe_w, const float *lepe_b, int lepe_ks,
+                       int dtype, void *out, void *stream);
+
 /* Bytes of the routing index [B, S*S, topk] int32; 0 on invalid sizes. */
 size_t bra_idx_workspace_bytes(int B, int S, int topk);
 

@@ -14,7 +14,7 @@ import os
 
 import torch
 
-__all__ = ["BraError", "route", "attend", "forward", "forward_host",
+__all__ = ["BraError", "route", "attend", "forward", "forward_static", "forward_host",
            "idx_workspace_bytes", "device_status", "library_path", "SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,6 +29,7 @@ SYMBOLS = {
     "bra_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "bra_attend": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "bra_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
+    "bra_forward_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "bra_idx_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "bra_device_status": (_I, [_P, _I]),
     "bra_status_string": (ctypes.c_char_p, [_I]),
@@ -142,6 +143,28 @@ def forward(q, k, v, heads: int, S: int, topk: int, lepe_w, lepe_b=None, out=Non
                              _ptr(idx), _ptr(out), _stream(stream))
     _check(rc, "bra_forward")
     return out, idx
+
+
+# Routing-index entries the library's built-in array holds (include/bra.h).
+STATIC_IDX_MAX_ENTRIES = 1 << 18
+
+
+def forward_static(q, k, v, heads: int, S: int, topk: int, lepe_w, lepe_b=None, out=None,
+                   stream=None):
+    """The whole BRA forward without a routing-index workspace, for callers
+    that may not allocate device memory: the index lives in an array inside
+    the library, shared by every call on the device (calls that overlap on the
+    GPU race on it). Returns out; B * S*S * topk must not exceed
+    STATIC_IDX_MAX_ENTRIES. The first call on a device looks the array up and
+    should come before any stream capture."""
+    B, H, W, C = _map(q, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    rc = _load().bra_forward_static(_ptr(q), _ptr(k), _ptr(v), B, H, W, C, heads, S, topk,
+                                    _ptr(lepe_w), _ptr(lepe_b), lepe_w.shape[-1],
+                                    _dtype_code(q), _ptr(out), _stream(stream))
+    _check(rc, "bra_forward_static")
+    return out
 
 
 class HostBuffers:

@@ -457,3 +457,57 @@ const char *bra_status_string(int status) {
 int bra_abi_version(void) { return 100; }
 
 }  // extern "C"
+
+// ------------------------------------------------- allocation-free forward
+// bra_forward_static keeps the routing index in this file-scope device array
+// instead of a caller-supplied workspace. Every GPU that loads the library
+// holds it (BRA_STATIC_IDX_MAX_ENTRIES int32, 1 MiB) until the process exits.
+namespace {
+
+__device__ __align__(256) int32_t g_static_idx[BRA_STATIC_IDX_MAX_ENTRIES];
+
+// Device address of g_static_idx, looked up once per device. In host code the
+// array's name is only a host-side stand-in, so kernels must be given this
+// address instead.
+int32_t *static_idx_address() {
+  constexpr int kMaxDevices = 64;
+  static int32_t *addr[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_idx) != cudaSuccess || !p) return nullptr;
+    addr[dev] = static_cast<int32_t *>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int bra_forward_static(const void *q, const void *k, const void *v, int B,
+                                  int H, int W, int C, int heads, int S, int topk,
+                                  const float *lepe_w, const float *lepe_b,
+                                  int lepe_ks, int dtype, void *out, void *stream) {
+  if (B > 0 && S > 0 && topk > 0 &&
+      (long long)B * S * S * topk > (long long)BRA_STATIC_IDX_MAX_ENTRIES)
+    return BRA_ERR_UNSUPPORTED;
+  // argument checks first, against a stand-in workspace pointer that cannot
+  // overlap a caller buffer's check (the real address is only known on the
+  // device); nothing is launched unless they pass
+  int rc = check_route(q, k, B, H, W, C, S, topk, dtype,
+                       reinterpret_cast<const int32_t *>(q));
+  if (rc) return rc;
+  rc = check_attend(q, k, v, reinterpret_cast<const int32_t *>(q), B, H, W, C, heads, S,
+                    topk, lepe_w, lepe_ks, dtype, out);
+  if (rc || B == 0) return rc;
+  int32_t *idx = static_idx_address();
+  if (!idx) return BRA_ERR_CUDA;
+  (void)cudaGetLastError();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_route(q, k, B, H, W, C, S, topk, dtype, idx, nullptr, s);
+  if (rc) return rc;
+  return launch_attend(q, k, v, idx, B, H, W, C, heads, S, topk, lepe_w, lepe_b,
+                       lepe_ks, dtype, out, true, s);
+}
