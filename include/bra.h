@@ -70,9 +70,9 @@ enum bra_dtype { BRA_F32 = 0, BRA_BF16 = 1 };
  *   idx       out: int32 [B, S*S, topk] device
  *   affinity  out (optional, may be NULL): float32 [B, S*S, S*S] device, the
  *             unscaled region affinity the selection was taken on
- * Supported: S*S <= 1024, B <= 65535, C % 8 == 0 (bf16) or C % 4 == 0
- * (f32), and 2 * ceil(S*S / 8) * C * 4 bytes of region means per CTA within
- * 200 KB; otherwise BRA_ERR_UNSUPPORTED.
+ * Supported: S*S <= 1024, B <= 65535, and C * element size a power of two
+ * from 16 to 512 bytes (bf16: C in {8, 16, ..., 256}; f32: C in {4, ..., 128});
+ * otherwise BRA_ERR_UNSUPPORTED.
  */
 int bra_route(const void *q, const void *k, int B, int H, int W, int C, int S,
               int topk, int dtype, int32_t *idx, float *affinity, void *stream);

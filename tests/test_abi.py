@@ -80,6 +80,8 @@ def test_route_argument_errors(lib):
     assert route(lib, dtype=7) == bra.BRA_ERR_INVALID_ARG
     assert route(lib, q=ctypes.c_void_p(0x10000004)) == bra.BRA_ERR_INVALID_ARG  # misaligned
     assert route(lib, C=60) == bra.BRA_ERR_UNSUPPORTED          # 16-byte channel groups
+    assert route(lib, C=96) == bra.BRA_ERR_UNSUPPORTED          # 12 groups: not a power of 2
+    assert route(lib, C=512) == bra.BRA_ERR_UNSUPPORTED         # 64 groups: more than 32
     assert route(lib, H=66, W=66, S=33, topk=1) == bra.BRA_ERR_UNSUPPORTED  # S^2 > 1024
     assert route(lib, B=0, q=NULL, k=NULL, idx=NULL) == bra.BRA_OK  # empty batch
 

@@ -23,7 +23,6 @@ using bra::AttendF32Geom;
 using bra::AttendGeom;
 
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;
-constexpr size_t kRouteSmemLimit = 200 * 1024;
 
 inline int elem_size(int dtype) { return dtype == BRA_F32 ? 4 : 2; }
 
@@ -73,22 +72,31 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 [B, H, W, C] map; box = 64 channels x box_w x box_h x 1 image,
-// zero fill outside the map; 128-byte swizzle for tiles read by ldmatrix.
-bool make_map(CUtensorMap *m, const void *base, int B, int H, int W, int C,
-              int box_w, int box_h, bool swizzle) {
+// [B, H, W, C] map of bf16 or f32; box = 128 bytes of channels x box_w x
+// box_h x 1 image, zero fill outside the map; 128-byte swizzle for tiles
+// read by ldmatrix.
+bool make_map_t(CUtensorMap *m, const void *base, int dtype, int B, int H, int W, int C,
+                int box_w, int box_h, bool swizzle) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  const cuuint64_t e = (cuuint64_t)elem_size(dtype);
   cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2,
-                           (cuuint64_t)H * W * C * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_w, (cuuint32_t)box_h, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)C * e, (cuuint64_t)W * C * e,
+                           (cuuint64_t)H * W * C * e};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / e), (cuuint32_t)box_w, (cuuint32_t)box_h, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  return enc(m, dtype == BRA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             4, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap *m, const void *base, int B, int H, int W, int C,
+              int box_w, int box_h, bool swizzle) {
+  return make_map_t(m, base, BRA_BF16, B, H, W, C, box_w, box_h, swizzle);
 }
 
 // Raises a kernel's dynamic shared-memory limit to the per-block maximum,
@@ -106,24 +114,55 @@ cudaError_t allow_smem(const void *kernel, size_t bytes) {
 }
 
 // ------------------------------------------------------------------ route
-// Whether the route kernel can keep all K means in local shared memory.
-bool route_local_k(int R, int C) {
-  const int CL = std::min(bra::kRouteMaxCluster, R);
-  return bra::RouteSmem::floats(R, C, CL, true) * sizeof(float) <= kRouteSmemLimit;
+int sm_count();
+bool allow_wide_clusters(const void *kernel);
+
+// 16-byte channel groups per token, if a power of two no larger than 32.
+int route_groups(int C, int dtype) {
+  const int bytes = C * elem_size(dtype);
+  if (bytes % 16) return 0;
+  const int G = bytes / 16;
+  return (G <= 32 && (G & (G - 1)) == 0) ? G : 0;
 }
 
-template <typename T, int MAXJ, bool LOCAL_K>
-int launch_route_k(const void *q, const void *k, int B, int H, int W, int C,
-                   int S, int topk, int32_t *idx, float *aff, cudaStream_t s) {
-  const int R = S * S;
-  const int CL = std::min(bra::kRouteMaxCluster, R);
-  const size_t smem = bra::RouteSmem::floats(R, C, CL, LOCAL_K) * sizeof(float);
-  auto kern = bra::bra_route_kernel<T, MAXJ, LOCAL_K>;
+// Plans the route kernel for a cluster of CL CTAs; false if it cannot run.
+bool plan_route(int B, int H, int W, int C, int S, int topk, int dtype, int CL,
+                bra::RouteGeom *g, size_t *smem, bool *local_k) {
+  (void)B;
+  bra::RouteGeom a = {};
+  a.H = H; a.W = W; a.C = C; a.S = S; a.topk = topk;
+  a.hr = H / S; a.wr = W / S; a.n = a.hr * a.wr; a.R = S * S;
+  a.G = route_groups(C, dtype);
+  if (!a.G) return false;
+  const int ro_max = (a.R + CL - 1) / CL;
+  const size_t means = (size_t)ro_max * C * 4;
+  const size_t kall = (size_t)a.R * (C + 1) * 4;
+  a.off_qm = 0;
+  a.off_km = (uint32_t)means;
+  a.off_kall = (uint32_t)round_up(2 * means, 16);
+  // a local copy of all K means whenever it fits: remote reads in the
+  // affinity loop cost far more than fewer CTAs per SM
+  *local_k = a.off_kall + kall <= kMaxSmemPerBlock;
+  *smem = a.off_kall + (*local_k ? kall : 0);
+  *g = a;
+  return *smem <= kMaxSmemPerBlock;
+}
+
+// Threads per route CTA: few clusters get 1024-thread CTAs.
+int route_threads(int B, int CL) {
+  return B * CL >= 2 * sm_count() ? bra::kRouteThreadsMany : bra::kRouteThreadsFew;
+}
+
+template <typename T, int MAXJ, bool LOCAL_K, int NT>
+int launch_route_n(const void *q, const void *k, int B, int CL, const bra::RouteGeom &g,
+                   size_t smem, int32_t *idx, float *aff, cudaStream_t s) {
+  auto kern = bra::bra_route_kernel<T, MAXJ, LOCAL_K, NT>;
   cudaError_t e = allow_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return BRA_ERR_CUDA;
+  if (CL > 8 && !allow_wide_clusters(reinterpret_cast<const void *>(kern))) return BRA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, B, 1);
-  cfg.blockDim = dim3(bra::kRouteThreads, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -133,29 +172,101 @@ int launch_route_k(const void *q, const void *k, int B, int H, int W, int C,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T *>(q),
-                         static_cast<const T *>(k), H, W, C, S, topk, idx, aff);
+  e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T *>(q), static_cast<const T *>(k), g,
+                         idx, aff);
   return cuda_status(e);
 }
 
+template <typename T, int MAXJ, bool LOCAL_K>
+int launch_route_k(const void *q, const void *k, int B, int CL, const bra::RouteGeom &g,
+                   size_t smem, int32_t *idx, float *aff, cudaStream_t s) {
+  if (route_threads(B, CL) == bra::kRouteThreadsMany)
+    return launch_route_n<T, MAXJ, LOCAL_K, bra::kRouteThreadsMany>(q, k, B, CL, g, smem, idx,
+                                                                      aff, s);
+  return launch_route_n<T, MAXJ, LOCAL_K, bra::kRouteThreadsFew>(q, k, B, CL, g, smem, idx,
+                                                                   aff, s);
+}
+
 template <typename T, int MAXJ>
-int launch_route_t(const void *q, const void *k, int B, int H, int W, int C,
-                   int S, int topk, int32_t *idx, float *aff, cudaStream_t s) {
-  if (route_local_k(S * S, C))
-    return launch_route_k<T, MAXJ, true>(q, k, B, H, W, C, S, topk, idx, aff, s);
-  return launch_route_k<T, MAXJ, false>(q, k, B, H, W, C, S, topk, idx, aff, s);
+int launch_route_t(const void *q, const void *k, int B, int CL, const bra::RouteGeom &g,
+                   size_t smem, bool local_k, int32_t *idx, float *aff, cudaStream_t s) {
+  if (local_k) return launch_route_k<T, MAXJ, true>(q, k, B, CL, g, smem, idx, aff, s);
+  return launch_route_k<T, MAXJ, false>(q, k, B, CL, g, smem, idx, aff, s);
 }
 
 template <typename T>
-int launch_route_dtype(const void *q, const void *k, int B, int H, int W, int C,
-                       int S, int topk, int32_t *idx, float *aff, cudaStream_t s) {
-  const int R = S * S;
-  if (R <= 32) return launch_route_t<T, 1>(q, k, B, H, W, C, S, topk, idx, aff, s);
-  if (R <= 64) return launch_route_t<T, 2>(q, k, B, H, W, C, S, topk, idx, aff, s);
-  if (R <= 128) return launch_route_t<T, 4>(q, k, B, H, W, C, S, topk, idx, aff, s);
-  if (R <= 256) return launch_route_t<T, 8>(q, k, B, H, W, C, S, topk, idx, aff, s);
-  if (R <= 512) return launch_route_t<T, 16>(q, k, B, H, W, C, S, topk, idx, aff, s);
-  return launch_route_t<T, 32>(q, k, B, H, W, C, S, topk, idx, aff, s);
+int launch_route_dtype(const void *q, const void *k, int B, int CL, const bra::RouteGeom &g,
+                       size_t smem, bool local_k, int32_t *idx, float *aff, cudaStream_t s) {
+  const int R = g.R;
+  if (R <= 32) return launch_route_t<T, 1>(q, k, B, CL, g, smem, local_k, idx, aff, s);
+  if (R <= 64) return launch_route_t<T, 2>(q, k, B, CL, g, smem, local_k, idx, aff, s);
+  if (R <= 128) return launch_route_t<T, 4>(q, k, B, CL, g, smem, local_k, idx, aff, s);
+  if (R <= 256) return launch_route_t<T, 8>(q, k, B, CL, g, smem, local_k, idx, aff, s);
+  if (R <= 512) return launch_route_t<T, 16>(q, k, B, CL, g, smem, local_k, idx, aff, s);
+  return launch_route_t<T, 32>(q, k, B, CL, g, smem, local_k, idx, aff, s);
+}
+
+// Lets a kernel use clusters of 16 CTAs (once per kernel and process).
+bool allow_wide_clusters(const void *kernel) {
+  static std::mutex mu;
+  static std::vector<const void *> done;
+  std::lock_guard<std::mutex> lock(mu);
+  if (std::find(done.begin(), done.end(), kernel) != done.end()) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+      cudaSuccess)
+    return false;
+  done.push_back(kernel);
+  return true;
+}
+
+// Whether clusters of 16 route CTAs with this much shared memory can be
+// resident on the current device (asked once per device, dtype and size).
+bool wide_clusters_ok(int dtype, size_t smem) {
+  struct Entry { int dev, dtype; size_t smem; bool ok; };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &e : cache)
+      if (e.dev == dev && e.dtype == dtype && e.smem == smem) return e.ok;
+  }
+  const void *kern = dtype == BRA_F32
+      ? reinterpret_cast<const void *>(
+            bra::bra_route_kernel<float, 8, true, bra::kRouteThreadsFew>)
+      : reinterpret_cast<const void *>(
+            bra::bra_route_kernel<__nv_bfloat16, 8, true, bra::kRouteThreadsFew>);
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, 1, 1);
+  cfg.blockDim = dim3(bra::kRouteThreadsFew, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const bool ok = allow_smem(kern, smem) == cudaSuccess && allow_wide_clusters(kern) &&
+                  cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0;
+  (void)cudaGetLastError();
+  std::lock_guard<std::mutex> lock(mu);
+  cache.push_back({dev, dtype, smem, ok});
+  return ok;
+}
+
+// Cluster size: 8 CTAs per image, 16 when the batch is too small to fill the
+// GPU with 8-CTA clusters and the device allows clusters of 16.
+int route_cluster(int B, int R, int H, int W, int C, int S, int topk, int dtype) {
+  const int CL = std::min(8, R);
+  if (R < 16 || B * 8 >= sm_count()) return CL;
+  bra::RouteGeom g;
+  size_t smem;
+  bool lk;
+  if (!plan_route(B, H, W, C, S, topk, dtype, 16, &g, &smem, &lk)) return CL;
+  return wide_clusters_ok(dtype, smem) ? 16 : CL;
 }
 
 int check_route(const void *q, const void *k, int B, int H, int W, int C, int S,
@@ -167,18 +278,24 @@ int check_route(const void *q, const void *k, int B, int H, int W, int C, int S,
   if (!aligned16(q) || !aligned16(k)) return BRA_ERR_INVALID_ARG;
   const int R = S * S;
   if (R > 1024 || B > 65535) return BRA_ERR_UNSUPPORTED;
-  if (C % (dtype == BRA_F32 ? 4 : 8)) return BRA_ERR_UNSUPPORTED;
-  const int CL = std::min(bra::kRouteMaxCluster, R);
-  if (bra::RouteSmem::floats(R, C, CL, false) * sizeof(float) > kRouteSmemLimit)
+  bra::RouteGeom g;
+  size_t smem;
+  bool lk;
+  if (!plan_route(B, H, W, C, S, topk, dtype, std::min(8, R), &g, &smem, &lk))
     return BRA_ERR_UNSUPPORTED;
   return BRA_OK;
 }
 
 int launch_route(const void *q, const void *k, int B, int H, int W, int C, int S,
                  int topk, int dtype, int32_t *idx, float *aff, cudaStream_t s) {
+  const int CL = route_cluster(B, S * S, H, W, C, S, topk, dtype);
+  bra::RouteGeom g;
+  size_t smem;
+  bool local_k;
+  if (!plan_route(B, H, W, C, S, topk, dtype, CL, &g, &smem, &local_k)) return BRA_ERR_UNSUPPORTED;
   if (dtype == BRA_F32)
-    return launch_route_dtype<float>(q, k, B, H, W, C, S, topk, idx, aff, s);
-  return launch_route_dtype<__nv_bfloat16>(q, k, B, H, W, C, S, topk, idx, aff, s);
+    return launch_route_dtype<float>(q, k, B, CL, g, smem, local_k, idx, aff, s);
+  return launch_route_dtype<__nv_bfloat16>(q, k, B, CL, g, smem, local_k, idx, aff, s);
 }
 
 // ----------------------------------------------------------------- attend
@@ -220,26 +337,37 @@ bool plan_attend_bf16(int B, int H, int W, int C, int heads, int S, int topk, in
   a.kv_chunk = (uint32_t)a.kv_rows * 128u;
   a.h_chunk = (uint32_t)a.halo_w * a.halo_h * 128u;
   a.o_chunk = (uint32_t)a.n * 128u;
+  a.tasks = heads * a.q_blocks;
   a.off_k = a.nc * a.q_chunk;
   a.off_v = a.off_k + a.nc * a.kv_chunk;
   a.off_h = a.off_v + a.nc * a.kv_chunk;
-  a.stage_bytes = (uint32_t)round_up((size_t)a.off_h + (size_t)a.nc * a.h_chunk, 1024);
+  const size_t halo_end = (size_t)a.off_h + (size_t)a.nc * a.h_chunk;
+  const size_t o_bytes = round_up((size_t)a.n * C * 4, 1024);
+  // O may overwrite the unit's Q/K/V once attention is done with them, unless
+  // padded K/V rows must stay zero or a warp would have to hold more than one
+  // task's O
+  a.alias = !a.masked && a.tasks <= bra::kGroupWarps && o_bytes <= a.off_h;
+  if (a.alias) {
+    a.off_o = 0;
+    a.stage_bytes = (uint32_t)round_up(halo_end, 1024);
+  } else {
+    a.off_o = (uint32_t)round_up(halo_end, 1024);
+    a.stage_bytes = (uint32_t)round_up((size_t)a.off_o + o_bytes, 1024);
+  }
   a.tx_bytes = a.nc * (a.o_chunk * (1u + 2u * topk) + a.h_chunk);
-  a.o_stride = C + 8;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
-  const size_t fixed = round_up((size_t)2 * a.nc * a.o_chunk, 1024) +
-                       round_up((size_t)a.n * a.o_stride * 4, 16) +
-                       round_up((size_t)(ks * ks + 1) * C * 4, 16) +
-                       2 * bra::kMaxStages * 8;
+  const size_t out_bytes = round_up((size_t)bra::kGroups * 2 * a.nc * a.o_chunk, 1024);
+  const size_t w_bytes = round_up((size_t)(ks * ks + 1) * C * 4, 16);
+  const size_t bar_bytes = bra::kMaxStages * 8;
   const size_t budget = kMaxSmemPerBlock - 1024;
+  const size_t fixed = out_bytes + w_bytes + bar_bytes;
   if (fixed + a.stage_bytes > budget) return false;
   a.stages = (int)std::min<size_t>(bra::kMaxStages, (budget - fixed) / a.stage_bytes);
-  size_t off = (size_t)a.stages * a.stage_bytes;
-  a.off_out = (uint32_t)off; off += round_up((size_t)2 * a.nc * a.o_chunk, 1024);
-  a.off_o = (uint32_t)off; off += round_up((size_t)a.n * a.o_stride * 4, 16);
-  a.off_w = (uint32_t)off; off += round_up((size_t)(ks * ks + 1) * C * 4, 16);
-  a.off_bar = (uint32_t)off; off += 2 * bra::kMaxStages * 8;
-  *smem = off + 1024;  // slack to align the base to 1024 bytes
+  if (a.stages > 1) a.stages &= ~1;  // an even count: each group owns half
+  a.off_out = (uint32_t)((size_t)a.stages * a.stage_bytes);
+  a.off_w = (uint32_t)(a.off_out + out_bytes);
+  a.off_bar = (uint32_t)(a.off_w + w_bytes);
+  *smem = (size_t)a.off_bar + bar_bytes + 1024;  // slack to align the base to 1024 bytes
   *g = a;
   return *smem <= kMaxSmemPerBlock;
 }
@@ -265,7 +393,7 @@ bool plan_attend_f32(int H, int W, int C, int heads, int S, int topk, int ks,
   return *smem <= kMaxSmemPerBlock;
 }
 
-template <int KS, int RB>
+template <int KS, int RB, int WR, int HR>
 int launch_attend_bf16_kr(const void *q, const void *k, const void *v,
                           const int32_t *idx, int B, const float *w,
                           const float *bias, void *out, const AttendGeom &g,
@@ -277,7 +405,7 @@ int launch_attend_bf16_kr(const void *q, const void *k, const void *v,
       !make_map(&th, v, B, g.H, g.W, g.C, g.halo_w, g.halo_h, false) ||
       !make_map(&to, out, B, g.H, g.W, g.C, g.wr, g.hr, false))
     return BRA_ERR_CUDA;
-  auto kern = bra::bra_attend_bf16_kernel<KS, RB>;
+  auto kern = bra::bra_attend_bf16_kernel<KS, RB, WR, HR>;
   if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
     return BRA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -298,11 +426,21 @@ int launch_attend_bf16_ks(const void *q, const void *k, const void *v,
                           const int32_t *idx, int B, const float *w,
                           const float *bias, void *out, const AttendGeom &g,
                           size_t smem, bool pdl, cudaStream_t s) {
+  // square regions of the stage shapes get their geometry at compile time
+  if constexpr (KS == 5) {
+    if (g.wr == g.hr && (g.wr == 8 || g.wr == 4 || g.wr == 2)) {
+      switch (g.wr) {
+      case 8: return launch_attend_bf16_kr<KS, 8, 8, 8>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+      case 4: return launch_attend_bf16_kr<KS, 4, 4, 4>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+      default: return launch_attend_bf16_kr<KS, 2, 2, 2>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+      }
+    }
+  }
   switch (lepe_row_block(g.hr)) {
-    case 8: return launch_attend_bf16_kr<KS, 8>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
-    case 4: return launch_attend_bf16_kr<KS, 4>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
-    case 2: return launch_attend_bf16_kr<KS, 2>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
-    default: return launch_attend_bf16_kr<KS, 1>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+    case 8: return launch_attend_bf16_kr<KS, 8, 0, 0>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+    case 4: return launch_attend_bf16_kr<KS, 4, 0, 0>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+    case 2: return launch_attend_bf16_kr<KS, 2, 0, 0>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+    default: return launch_attend_bf16_kr<KS, 1, 0, 0>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
   }
 }
 

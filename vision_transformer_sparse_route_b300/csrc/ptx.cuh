@@ -66,9 +66,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Waits for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
 // On giving up it sets kStatusTimeout and returns false; the caller carries
-// on (so that every thread still reaches every barrier of the block).
+// on (so that every thread still reaches every barrier of the block). Once
+// the timeout bit is set (until the host clears it), waits that do not
+// succeed at once return false immediately, so a launch that went wrong ends
+// quickly instead of timing out wait by wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
+  // after one wait of this launch has given up, later ones do not wait again
+  if (*reinterpret_cast<volatile unsigned *>(&g_status) & kStatusTimeout) return false;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
     if (global_ns() - t0 > kWaitLimitNs) {

@@ -6,14 +6,17 @@
 // A_r = q_r k_r^T, I_r = topk(A_r); page "从静态到动态：BRA双层路由注意力
 // 如何革新视觉Transformer的计算范式" §2 mean pooling and §4 TopkRouting).
 //
-// One thread-block cluster per image. Each CTA of the cluster pools a share
-// of the regions (regions r with r % CL == rank) into its shared memory, the
-// cluster synchronises, every CTA copies all K means out of its peers' shared
-// memory (distributed shared memory; for grids too large to copy, it reads
-// them from the peers in place), and then computes the affinity rows and the
-// top-k of its own query regions. Nothing goes through global memory but
-// the inputs and the outputs. Arithmetic is float32 with FMA in a fixed
-// channel order.
+// One thread-block cluster per image. Each CTA of the cluster owns the
+// regions r with r % CL == rank. One warp pools one (tensor, region): a
+// region's rows are contiguous runs of wr*C elements, read with 16-byte loads
+// that a lane issues back to back (every lane always lands on the same 16-byte
+// channel group, since a token holds a power-of-two number of them), then a
+// few shuffles sum the lanes of each group. Then the cluster synchronises,
+// every CTA copies all K means out of its peers' shared memory (distributed
+// shared memory; for grids too large to copy, it reads them from the peers in
+// place), and computes the affinity rows and the top-k of its own regions.
+// Nothing goes through global memory but the inputs and the outputs.
+// Arithmetic is float32 with FMA in a fixed order.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -24,46 +27,48 @@ namespace bra {
 
 namespace cg = cooperative_groups;
 
-constexpr int kRouteThreads = 256;
-constexpr int kRouteMaxCluster = 8;
+// Threads per CTA: 256 when there are enough clusters to fill the GPU (four
+// CTAs per SM), 1024 when there are few (one CTA per SM, one warp per pooled
+// region).
+constexpr int kRouteThreadsMany = 256;
+constexpr int kRouteThreadsFew = 1024;
+constexpr int kRouteUnroll = 8;  // 16-byte loads a lane keeps in flight
+
+struct RouteGeom {
+  int H, W, C, S, topk;
+  int hr, wr, n, R;
+  int G;        // 16-byte channel groups per token (a power of two <= 32)
+  uint32_t off_qm, off_km, off_kall;  // bytes into shared memory
+};
 
 template <typename T> struct Vec16;
 template <> struct Vec16<float> {
   static constexpr int N = 4;
-  __device__ static void load(const float *p, float (&o)[4]) {
-    float4 v = __ldg(reinterpret_cast<const float4 *>(p));
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  __device__ static void add(const uint4 &v, float (&acc)[8]) {
+    acc[0] += __uint_as_float(v.x); acc[1] += __uint_as_float(v.y);
+    acc[2] += __uint_as_float(v.z); acc[3] += __uint_as_float(v.w);
   }
 };
 template <> struct Vec16<__nv_bfloat16> {
   static constexpr int N = 8;
-  __device__ static void load(const __nv_bfloat16 *p, float (&o)[8]) {
-    uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
-    o[0] = bf16_lo(v.x); o[1] = bf16_hi(v.x);
-    o[2] = bf16_lo(v.y); o[3] = bf16_hi(v.y);
-    o[4] = bf16_lo(v.z); o[5] = bf16_hi(v.z);
-    o[6] = bf16_lo(v.w); o[7] = bf16_hi(v.w);
+  __device__ static void add(const uint4 &v, float (&acc)[8]) {
+    acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
+    acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+    acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
+    acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
   }
 };
 
-// Shared-memory floats of the route kernel: own Q and K means, plus (when
-// the K means of all regions are copied locally) an [R][C+1] table.
-struct RouteSmem {
-  __host__ __device__ static size_t floats(int R, int C, int CL, bool local_k) {
-    const size_t ro_max = (size_t)(R + CL - 1) / CL;
-    return 2 * ro_max * C + (local_k ? (size_t)R * (C + 1) : 0);
-  }
-};
-
-// Grid (CL, B), cluster (CL, 1, 1), kRouteThreads threads.
+// Grid (CL, B), cluster (CL, 1, 1), NT threads.
 // MAXJ = ceil(R / 32): affinity values each lane keeps for the top-k.
 // LOCAL_K: copy every K mean into local shared memory first (fast path);
 // otherwise read them from the peers' shared memory in the affinity loop.
-template <typename T, int MAXJ, bool LOCAL_K>
-__global__ void __launch_bounds__(kRouteThreads)
-    bra_route_kernel(const T *__restrict__ q, const T *__restrict__ k, int H,
-                     int W, int C, int S, int topk, int32_t *__restrict__ idx,
-                     float *__restrict__ affinity) {
+// At most 64 registers a thread (4 CTAs of 256 or one of 1024 per SM), except
+// for grids of more than 256 regions, whose rows keep more values a lane.
+template <typename T, int MAXJ, bool LOCAL_K, int NT>
+__global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
+    bra_route_kernel(const T *__restrict__ q, const T *__restrict__ k, RouteGeom g,
+                     int32_t *__restrict__ idx, float *__restrict__ affinity) {
   // A dependent grid launched with programmatic serialization may start now;
   // it waits for this grid before it reads the routing index.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -71,91 +76,102 @@ __global__ void __launch_bounds__(kRouteThreads)
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
   const int b = blockIdx.y;
-  const int R = S * S, hr = H / S, wr = W / S, n = hr * wr;
-  const int ro = (R - rank + CL - 1) / CL;  // regions rank, rank+CL, ...
-  const int ro_max = (R + CL - 1) / CL;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kWarps = kRouteThreads / 32;
+  const int R = g.R, C = g.C;
+  const int ro = (R - rank + CL - 1) / CL;  // owned regions rank, rank+CL, ...
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int VEC = Vec16<T>::N;
 
-  extern __shared__ __align__(16) float route_smem[];
-  float *qm = route_smem;            // [ro_max][C] own query-region means
-  float *km = qm + ro_max * C;       // [ro_max][C] own key-region means
-  float *kall = km + ro_max * C;     // [R][C+1] all key-region means
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  float *qm = reinterpret_cast<float *>(route_smem + g.off_qm);      // [ro_max][C]
+  float *km = reinterpret_cast<float *>(route_smem + g.off_km);      // [ro_max][C]
+  float *kall = reinterpret_cast<float *>(route_smem + g.off_kall);  // [R][C+1]
 
   // ---- 1. region means of q and k: one warp per (tensor, owned region) ----
-  constexpr int VEC = Vec16<T>::N;
-  const int G = C / VEC;                       // 16-byte groups per token
-  const int GW = G < 32 ? G : 32;              // lanes across channel groups
-  int TL = 1;                                  // lanes across tokens (pow2)
-  while (TL * 2 * GW <= 32) TL *= 2;
-  const int tl = lane / GW, gl = lane % GW;
-  const bool active = lane < TL * GW;
-  const float inv_n = 1.0f / static_cast<float>(n);
-  for (int task = warp; task < 2 * ro; task += kWarps) {
+  const int seg = g.wr * g.G;       // 16-byte chunks in one region row
+  const int total = g.hr * seg;     // chunks in the region
+  const size_t row_stride = (size_t)g.W * g.G;
+  const float inv_n = 1.0f / static_cast<float>(g.n);
+  for (int task = warp; task < 2 * ro; task += NT / 32) {
     const int tensor = task & 1, s = task >> 1;
     const int r = rank + CL * s;
-    const int y0 = (r / S) * hr, x0 = (r % S) * wr;
-    const T *src = (tensor ? k : q) + (size_t)b * H * W * C;
-    float *dst = (tensor ? km : qm) + s * C;
-    for (int g0 = 0; g0 < G; g0 += GW) {
-      float acc[VEC];
+    const int y0 = (r / g.S) * g.hr, x0 = (r % g.S) * g.wr;
+    const uint4 *base = reinterpret_cast<const uint4 *>(tensor ? k : q) +
+                        (((size_t)b * g.H + y0) * g.W + x0) * g.G;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // chunk lane + 32 j of the region: row and column kept incrementally
+    int row = lane / seg, col = lane % seg;
+    for (int j0 = lane; j0 < total; j0 += 32 * kRouteUnroll) {
+      uint4 v[kRouteUnroll];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
-      const int g = g0 + gl;
-      if (active && g < G) {
-#pragma unroll 8
-        for (int t = tl; t < n; t += TL) {
-          const int y = y0 + t / wr, x = x0 + t % wr;
-          float v[VEC];
-          Vec16<T>::load(src + ((size_t)y * W + x) * C + g * VEC, v);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[e] += v[e];
+      for (int u = 0; u < kRouteUnroll; ++u) {
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (j0 + 32 * u < total) v[u] = __ldg(base + row * row_stride + col);
+        col += 32;
+        while (col >= seg) {
+          col -= seg;
+          ++row;
         }
       }
-      // sum the TL token lanes of each channel group (lanes gl, gl+GW, ...)
-      for (int off = GW; off < TL * GW; off <<= 1)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-      if (active && tl == 0 && g < G)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) dst[g * VEC + e] = acc[e] * inv_n;
+      for (int u = 0; u < kRouteUnroll; ++u) Vec16<T>::add(v[u], acc);
     }
+    // lanes l and l + G, l + 2G, ... hold the same channel group
+    for (int off = g.G; off < 32; off <<= 1)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    float *dst = (tensor ? km : qm) + s * C;
+    if (lane < g.G)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) dst[lane * VEC + e] = acc[e] * inv_n;
   }
 
   cluster.sync();
 
   // ---- 2. gather every region's K mean from the cluster ----
   if (LOCAL_K) {
-    for (int e = threadIdx.x; e < R * C; e += kRouteThreads) {
-      const int r = e / C, c = e % C;
+    const int c4n = C / 4;
+    for (int e = tid; e < R * c4n; e += NT) {
+      const int r = e / c4n, c4 = e % c4n;
       const float *peer = cluster.map_shared_rank(km, r % CL);
-      kall[r * (C + 1) + c] = peer[(r / CL) * C + c];
+      const float4 v = *reinterpret_cast<const float4 *>(peer + (r / CL) * C + 4 * c4);
+      float *d = kall + r * (C + 1) + 4 * c4;
+      d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
     }
     cluster.sync();  // peers are done reading our km; kall complete
   }
 
   // ---- 3. affinity rows and top-k: one warp per owned query region ----
-  for (int s = warp; s < ro; s += kWarps) {
+  for (int s = warp; s < ro; s += NT / 32) {
     const int i = rank + CL * s;
     const float *qi = qm + s * C;
+    const float *kj[MAXJ];
+#pragma unroll
+    for (int t = 0; t < MAXJ; ++t) {
+      const int j = min(lane + 32 * t, R - 1);
+      kj[t] = LOCAL_K ? kall + j * (C + 1)
+                      : cluster.map_shared_rank(km, j % CL) + (j / CL) * C;
+    }
+    float dot[MAXJ];
+#pragma unroll
+    for (int t = 0; t < MAXJ; ++t) dot[t] = 0.f;
+    for (int c = 0; c < C; ++c) {
+      const float qc = qi[c];
+#pragma unroll
+      for (int t = 0; t < MAXJ; ++t) dot[t] = fmaf(qc, kj[t][c], dot[t]);
+    }
     float val[MAXJ];
 #pragma unroll
     for (int t = 0; t < MAXJ; ++t) {
       const int j = lane + 32 * t;
       float a = -INFINITY;
       if (j < R) {
-        const float *kj = LOCAL_K ? kall + j * (C + 1)
-                                  : cluster.map_shared_rank(km, j % CL) + (j / CL) * C;
-        float dot = 0.f;
-        for (int c = 0; c < C; ++c) dot = fmaf(qi[c], kj[c], dot);
-        if (affinity) affinity[((size_t)b * R + i) * R + j] = dot;
-        a = (dot == dot) ? dot : -INFINITY;  // a NaN never wins
+        if (affinity) affinity[((size_t)b * R + i) * R + j] = dot[t];
+        a = (dot[t] == dot[t]) ? dot[t] : -INFINITY;  // a NaN never wins
       }
       val[t] = a;
     }
     unsigned taken = 0;  // bit t: column lane + 32 t already chosen
-    for (int m = 0; m < topk; ++m) {
+    for (int m = 0; m < g.topk; ++m) {
       float bv = -INFINITY;
       int bj = 0x7fffffff;
 #pragma unroll
@@ -177,7 +193,7 @@ __global__ void __launch_bounds__(kRouteThreads)
         }
       }
       if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
-      if (lane == 0) idx[((size_t)b * R + i) * topk + m] = bj;
+      if (lane == 0) idx[((size_t)b * R + i) * g.topk + m] = bj;
     }
   }
   if (!LOCAL_K) cluster.sync();  // keep km alive until every peer is done
