@@ -243,7 +243,7 @@ def our_arm(args, wl):
 
     # this rank's shard of a world * B image batch (weak scaling)
     wl_global = wl.replace(B=wl.B * world)
-    x = bra_synth.make_inputs(wl_global, seed=0, batch=slice(rank * wl.B, (rank + 1) * wl.B))
+    x = bra_synth.make_inputs(wl_global, seed=0, batch=bra_synth.rank_slice(wl.B, rank))
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     cast = lambda a: torch.from_numpy(a).to(tdt)
     host = [cast(a).pin_memory() for a in (x.q, x.k, x.v)]
@@ -332,20 +332,43 @@ def our_arm(args, wl):
     tokens = world * args.steps * wl.tokens
     value = tokens / (ms / 1e3)
 
-    # per-kernel durations (CUDA events around each launch on its stream)
+    # per-kernel durations: each kernel captured alone in a CUDA graph per input
+    # set and replayed back to back over the rotating sets (no host work between
+    # launches); CUDA events on the launching stream bracket the replays
     ks = max(1, args.kernel_steps)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(ks)]
-    with torch.cuda.stream(stream):
-        for i in range(ks):
-            q, k, v, out, idx = bufs[i % sets]
-            evs[i][0].record(stream)
-            bra.route(q, k, wl.S, wl.topk, idx=idx, stream=stream)
-            evs[i][1].record(stream)
-            bra.attend(q, k, v, idx, wl.heads, wl.S, w, b, out=out, stream=stream)
-            evs[i][2].record(stream)
-        stream.synchronize()
-    route_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / ks
-    attend_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / ks
+
+    def kernel_graphs(launch):
+        gs = []
+        with torch.cuda.stream(stream):
+            for s in range(sets):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    launch(s)
+                gs.append(g)
+        return gs
+
+    def time_graphs(gs):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                gs[i % sets].replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(ks):
+                gs[i % sets].replay()
+            e1.record(stream)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / ks
+
+    def launch_route(s):
+        q, k, v, out, idx = bufs[s]
+        bra.route(q, k, wl.S, wl.topk, idx=idx, stream=stream)
+
+    def launch_attend(s):
+        q, k, v, out, idx = bufs[s]
+        bra.attend(q, k, v, idx, wl.heads, wl.S, w, b, out=out, stream=stream)
+
+    route_ms = time_graphs(kernel_graphs(launch_route))
+    attend_ms = time_graphs(kernel_graphs(launch_attend))
 
     # end to end through the public API with pinned host buffers
     hb = bra.HostBuffers(host[0].shape, tdt, wl.S, wl.topk, dev)

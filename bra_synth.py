@@ -88,6 +88,12 @@ WORKLOADS = {
 }
 
 
+def rank_slice(per_rank: int, rank: int) -> slice:
+    """Images of a world * per_rank batch that rank `rank` draws and runs:
+    a contiguous block, so the shards of all ranks tile the batch."""
+    return slice(rank * per_rank, (rank + 1) * per_rank)
+
+
 def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
     """Outputs start+1 .. start+count of SplitMix64 seeded with `seed`."""
     i = np.arange(start + 1, start + count + 1, dtype=np.uint64)
