@@ -153,10 +153,18 @@ int route_threads(int B, int CL) {
   return B * CL >= 2 * sm_count() ? bra::kRouteThreadsMany : bra::kRouteThreadsFew;
 }
 
-template <typename T, int MAXJ, bool LOCAL_K, int NT>
-int launch_route_n(const void *q, const void *k, int B, int CL, const bra::RouteGeom &g,
+// Chunks of a region row per 32 lanes, when a whole multiple (1, 2 or 4), else 0.
+int route_row_chunks(const bra::RouteGeom &g) {
+  const int seg = g.wr * g.G;
+  if (seg % 32) return 0;
+  const int sw = seg / 32;
+  return (sw == 1 || sw == 2 || sw == 4) ? sw : 0;
+}
+
+template <typename T, int MAXJ, bool LOCAL_K, int NT, int SW>
+int launch_route_w(const void *q, const void *k, int B, int CL, const bra::RouteGeom &g,
                    size_t smem, int32_t *idx, float *aff, cudaStream_t s) {
-  auto kern = bra::bra_route_kernel<T, MAXJ, LOCAL_K, NT>;
+  auto kern = bra::bra_route_kernel<T, MAXJ, LOCAL_K, NT, SW>;
   cudaError_t e = allow_smem(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return BRA_ERR_CUDA;
   if (CL > 8 && !allow_wide_clusters(reinterpret_cast<const void *>(kern))) return BRA_ERR_CUDA;
@@ -175,6 +183,17 @@ int launch_route_n(const void *q, const void *k, int B, int CL, const bra::Route
   e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T *>(q), static_cast<const T *>(k), g,
                          idx, aff);
   return cuda_status(e);
+}
+
+template <typename T, int MAXJ, bool LOCAL_K, int NT>
+int launch_route_n(const void *q, const void *k, int B, int CL, const bra::RouteGeom &g,
+                   size_t smem, int32_t *idx, float *aff, cudaStream_t s) {
+  switch (route_row_chunks(g)) {
+    case 1: return launch_route_w<T, MAXJ, LOCAL_K, NT, 1>(q, k, B, CL, g, smem, idx, aff, s);
+    case 2: return launch_route_w<T, MAXJ, LOCAL_K, NT, 2>(q, k, B, CL, g, smem, idx, aff, s);
+    case 4: return launch_route_w<T, MAXJ, LOCAL_K, NT, 4>(q, k, B, CL, g, smem, idx, aff, s);
+    default: return launch_route_w<T, MAXJ, LOCAL_K, NT, 0>(q, k, B, CL, g, smem, idx, aff, s);
+  }
 }
 
 template <typename T, int MAXJ, bool LOCAL_K>
@@ -234,9 +253,9 @@ bool wide_clusters_ok(int dtype, size_t smem) {
   }
   const void *kern = dtype == BRA_F32
       ? reinterpret_cast<const void *>(
-            bra::bra_route_kernel<float, 8, true, bra::kRouteThreadsFew>)
+            bra::bra_route_kernel<float, 8, true, bra::kRouteThreadsFew, 0>)
       : reinterpret_cast<const void *>(
-            bra::bra_route_kernel<__nv_bfloat16, 8, true, bra::kRouteThreadsFew>);
+            bra::bra_route_kernel<__nv_bfloat16, 8, true, bra::kRouteThreadsFew, 0>);
   int n = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(16, 1, 1);

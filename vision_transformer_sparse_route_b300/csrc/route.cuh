@@ -44,20 +44,81 @@ struct RouteGeom {
 template <typename T> struct Vec16;
 template <> struct Vec16<float> {
   static constexpr int N = 4;
-  __device__ static void add(const uint4 &v, float (&acc)[8]) {
-    acc[0] += __uint_as_float(v.x); acc[1] += __uint_as_float(v.y);
-    acc[2] += __uint_as_float(v.z); acc[3] += __uint_as_float(v.w);
+  __device__ static void add(const uint4 &v, float2 (&acc)[4]) {
+    acc[0] = __fadd2_rn(acc[0], make_float2(__uint_as_float(v.x), __uint_as_float(v.y)));
+    acc[1] = __fadd2_rn(acc[1], make_float2(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
 };
 template <> struct Vec16<__nv_bfloat16> {
   static constexpr int N = 8;
-  __device__ static void add(const uint4 &v, float (&acc)[8]) {
-    acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
-    acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
-    acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
-    acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+  // the two bf16 of a word as a float pair, by byte permutes
+  __device__ static float2 pair(uint32_t w) {
+    return make_float2(__uint_as_float(__byte_perm(w, 0u, 0x1044u)),
+                       __uint_as_float(__byte_perm(w, 0u, 0x3244u)));
+  }
+  __device__ static void add(const uint4 &v, float2 (&acc)[4]) {
+    acc[0] = __fadd2_rn(acc[0], pair(v.x));
+    acc[1] = __fadd2_rn(acc[1], pair(v.y));
+    acc[2] = __fadd2_rn(acc[2], pair(v.z));
+    acc[3] = __fadd2_rn(acc[3], pair(v.w));
   }
 };
+
+// A streaming 16-byte load: not kept in L1, and L2 fetches the surrounding
+// 256 bytes (a region row is 1 KB or more of contiguous tokens).
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Sums this lane's 16-byte chunks of one region (rows of seg chunks, row
+// stride row_stride chunks; chunk lane + 32 m of the region). SW = seg / 32
+// when seg is a multiple of 32 (then chunk m of a lane sits at row m / SW,
+// column lane + 32 (m % SW), all offsets known at compile time); SW = 0 is
+// the general case.
+template <typename T, int SW>
+__device__ __forceinline__ void pool_region(const uint4 *base, size_t row_stride, int hr,
+                                            int seg, int lane, float2 (&acc)[4]) {
+  if constexpr (SW > 0) {
+    const uint4 *p = base + lane;
+    constexpr int RU = (SW <= 0 || SW >= kRouteUnroll) ? 1 : kRouteUnroll / SW;  // rows per batch
+    for (int y0 = 0; y0 < hr; y0 += RU) {
+      uint4 v[RU][SW];
+#pragma unroll
+      for (int y = 0; y < RU; ++y)
+#pragma unroll
+        for (int c = 0; c < SW; ++c)
+          v[y][c] = y0 + y < hr ? ld_stream16(p + (size_t)y * row_stride + 32 * c)
+                                : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int y = 0; y < RU; ++y)
+#pragma unroll
+        for (int c = 0; c < SW; ++c) Vec16<T>::add(v[y][c], acc);
+      p += RU * row_stride;
+    }
+    return;
+  }
+  const int total = hr * seg;
+  int row = lane / seg, col = lane % seg;
+  for (int j0 = lane; j0 < total; j0 += 32 * kRouteUnroll) {
+    uint4 v[kRouteUnroll];
+#pragma unroll
+    for (int u = 0; u < kRouteUnroll; ++u) {
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (j0 + 32 * u < total) v[u] = __ldg(base + row * row_stride + col);
+      col += 32;
+      while (col >= seg) {
+        col -= seg;
+        ++row;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRouteUnroll; ++u) Vec16<T>::add(v[u], acc);
+  }
+}
 
 // Grid (CL, B), cluster (CL, 1, 1), NT threads.
 // MAXJ = ceil(R / 32): affinity values each lane keeps for the top-k.
@@ -65,7 +126,7 @@ template <> struct Vec16<__nv_bfloat16> {
 // otherwise read them from the peers' shared memory in the affinity loop.
 // At most 64 registers a thread (4 CTAs of 256 or one of 1024 per SM), except
 // for grids of more than 256 regions, whose rows keep more values a lane.
-template <typename T, int MAXJ, bool LOCAL_K, int NT>
+template <typename T, int MAXJ, bool LOCAL_K, int NT, int SW>
 __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
     bra_route_kernel(const T *__restrict__ q, const T *__restrict__ k, RouteGeom g,
                      int32_t *__restrict__ idx, float *__restrict__ affinity) {
@@ -87,8 +148,7 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
   float *kall = reinterpret_cast<float *>(route_smem + g.off_kall);  // [R][C+1]
 
   // ---- 1. region means of q and k: one warp per (tensor, owned region) ----
-  const int seg = g.wr * g.G;       // 16-byte chunks in one region row
-  const int total = g.hr * seg;     // chunks in the region
+  const int seg = g.wr * g.G;  // 16-byte chunks in one region row
   const size_t row_stride = (size_t)g.W * g.G;
   const float inv_n = 1.0f / static_cast<float>(g.n);
   for (int task = warp; task < 2 * ro; task += NT / 32) {
@@ -97,24 +157,10 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
     const int y0 = (r / g.S) * g.hr, x0 = (r % g.S) * g.wr;
     const uint4 *base = reinterpret_cast<const uint4 *>(tensor ? k : q) +
                         (((size_t)b * g.H + y0) * g.W + x0) * g.G;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // chunk lane + 32 j of the region: row and column kept incrementally
-    int row = lane / seg, col = lane % seg;
-    for (int j0 = lane; j0 < total; j0 += 32 * kRouteUnroll) {
-      uint4 v[kRouteUnroll];
-#pragma unroll
-      for (int u = 0; u < kRouteUnroll; ++u) {
-        v[u] = make_uint4(0, 0, 0, 0);
-        if (j0 + 32 * u < total) v[u] = __ldg(base + row * row_stride + col);
-        col += 32;
-        while (col >= seg) {
-          col -= seg;
-          ++row;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kRouteUnroll; ++u) Vec16<T>::add(v[u], acc);
-    }
+    float2 acc2[4] = {};
+    pool_region<T, SW>(base, row_stride, g.hr, seg, lane, acc2);
+    float acc[8] = {acc2[0].x, acc2[0].y, acc2[1].x, acc2[1].y,
+                    acc2[2].x, acc2[2].y, acc2[3].x, acc2[3].y};
     // lanes l and l + G, l + 2G, ... hold the same channel group
     for (int off = g.G; off < 32; off <<= 1)
 #pragma unroll
