@@ -144,6 +144,14 @@ bool plan_route(int B, int H, int W, int C, int S, int topk, int dtype, int CL,
   // affinity loop cost far more than fewer CTAs per SM
   *local_k = a.off_kall + kall <= kMaxSmemPerBlock;
   *smem = a.off_kall + (*local_k ? kall : 0);
+  // the owned rows of the affinity, staged for the top-k, when they fit
+  const size_t aff = (size_t)ro_max * a.R * 4;
+  a.off_aff = 0;
+  if (*local_k && C % 4 == 0 &&
+      *smem + aff <= std::min<size_t>(kMaxSmemPerBlock, *smem + 48 * 1024)) {
+    a.off_aff = (uint32_t)round_up(*smem, 16);
+    *smem = a.off_aff + aff;
+  }
   *g = a;
   return *smem <= kMaxSmemPerBlock;
 }

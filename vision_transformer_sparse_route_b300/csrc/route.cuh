@@ -28,17 +28,20 @@ namespace bra {
 namespace cg = cooperative_groups;
 
 // Threads per CTA: 256 when there are enough clusters to fill the GPU (four
-// CTAs per SM), 1024 when there are few (one CTA per SM, one warp per pooled
-// region).
+// CTAs per SM), 512 when there are few (more warps per image; clusters of 16
+// such CTAs still pack several to a GPC).
 constexpr int kRouteThreadsMany = 256;
-constexpr int kRouteThreadsFew = 1024;
+constexpr int kRouteThreadsFew = 512;
 constexpr int kRouteUnroll = 8;  // 16-byte loads a lane keeps in flight
+
+constexpr int kAffRows = 4;  // owned rows of one affinity tile
 
 struct RouteGeom {
   int H, W, C, S, topk;
   int hr, wr, n, R;
   int G;        // 16-byte channel groups per token (a power of two <= 32)
   uint32_t off_qm, off_km, off_kall;  // bytes into shared memory
+  uint32_t off_aff;  // owned affinity rows [ro][R] (0: rows not staged)
 };
 
 template <typename T> struct Vec16;
@@ -186,24 +189,65 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
     cluster.sync();  // peers are done reading our km; kall complete
   }
 
-  // ---- 3. affinity rows and top-k: one warp per owned query region ----
+  // ---- 3. affinity rows and top-k ----
+  float *arow = reinterpret_cast<float *>(route_smem + g.off_aff);  // [ro][R]
+  if (LOCAL_K && g.off_aff) {
+    // tiles of kAffRows owned rows x 32 columns (lane = column j), spread over
+    // all warps: per four channels, four K-mean values of the lane's column
+    // and one broadcast 16-byte load of each row's Q mean; the FMAs still run
+    // channel by channel in order
+    const int rtiles = (ro + kAffRows - 1) / kAffRows, ctiles = (R + 31) / 32;
+    for (int t = warp; t < rtiles * ctiles; t += NT / 32) {
+      const int r0 = (t / ctiles) * kAffRows, j = (t % ctiles) * 32 + lane;
+      const float *kj = kall + min(j, R - 1) * (C + 1);
+      const float *q0 = qm + min(r0, ro - 1) * C;
+      float acc[kAffRows];
+#pragma unroll
+      for (int r = 0; r < kAffRows; ++r) acc[r] = 0.f;
+#pragma unroll 2
+      for (int c = 0; c < C; c += 4) {
+        const float k0 = kj[c], k1 = kj[c + 1], k2 = kj[c + 2], k3 = kj[c + 3];
+#pragma unroll
+        for (int r = 0; r < kAffRows; ++r) {
+          // rows past the owned ones repeat the last (their results are dropped)
+          const float4 q4 = *reinterpret_cast<const float4 *>(
+              q0 + (r0 + r < ro ? r : 0) * C + c);
+          float a = fmaf(q4.x, k0, acc[r]);
+          a = fmaf(q4.y, k1, a);
+          a = fmaf(q4.z, k2, a);
+          acc[r] = fmaf(q4.w, k3, a);
+        }
+      }
+      if (j < R)
+#pragma unroll
+        for (int r = 0; r < kAffRows; ++r)
+          if (r0 + r < ro) arow[(r0 + r) * R + j] = acc[r];
+    }
+    __syncthreads();
+  }
   for (int s = warp; s < ro; s += NT / 32) {
     const int i = rank + CL * s;
-    const float *qi = qm + s * C;
-    const float *kj[MAXJ];
-#pragma unroll
-    for (int t = 0; t < MAXJ; ++t) {
-      const int j = min(lane + 32 * t, R - 1);
-      kj[t] = LOCAL_K ? kall + j * (C + 1)
-                      : cluster.map_shared_rank(km, j % CL) + (j / CL) * C;
-    }
     float dot[MAXJ];
+    if (LOCAL_K && g.off_aff) {
 #pragma unroll
-    for (int t = 0; t < MAXJ; ++t) dot[t] = 0.f;
-    for (int c = 0; c < C; ++c) {
-      const float qc = qi[c];
+      for (int t = 0; t < MAXJ; ++t) dot[t] = arow[s * R + min(lane + 32 * t, R - 1)];
+    } else {
+      // one warp per row, lanes over columns (rows too long to stage)
+      const float *qi = qm + s * C;
+      const float *kj[MAXJ];
 #pragma unroll
-      for (int t = 0; t < MAXJ; ++t) dot[t] = fmaf(qc, kj[t][c], dot[t]);
+      for (int t = 0; t < MAXJ; ++t) {
+        const int j = min(lane + 32 * t, R - 1);
+        kj[t] = LOCAL_K ? kall + j * (C + 1)
+                        : cluster.map_shared_rank(km, j % CL) + (j / CL) * C;
+      }
+#pragma unroll
+      for (int t = 0; t < MAXJ; ++t) dot[t] = 0.f;
+      for (int c = 0; c < C; ++c) {
+        const float qc = qi[c];
+#pragma unroll
+        for (int t = 0; t < MAXJ; ++t) dot[t] = fmaf(qc, kj[t][c], dot[t]);
+      }
     }
     float val[MAXJ];
 #pragma unroll
@@ -215,6 +259,29 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
         a = (dot[t] == dot[t]) ? dot[t] : -INFINITY;  // a NaN never wins
       }
       val[t] = a;
+    }
+    if (LOCAL_K && g.off_aff && R <= 64 && g.topk > 4) {
+      // small grids, many routed regions: the rank of each of the lane's values in the row
+      // (larger values first, equal values by lower column) is its place in
+      // the top-k; one broadcast load per column, no shuffles
+      int rank_of[MAXJ];
+#pragma unroll
+      for (int t = 0; t < MAXJ; ++t) rank_of[t] = 0;
+      for (int jj = 0; jj < R; ++jj) {
+        float a = arow[s * R + jj];
+        a = (a == a) ? a : -INFINITY;
+#pragma unroll
+        for (int t = 0; t < MAXJ; ++t) {
+          const int j = lane + 32 * t;
+          rank_of[t] += (a > val[t] || (a == val[t] && jj < j)) ? 1 : 0;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MAXJ; ++t) {
+        const int j = lane + 32 * t;
+        if (j < R && rank_of[t] < g.topk) idx[((size_t)b * R + i) * g.topk + rank_of[t]] = j;
+      }
+      continue;
     }
     unsigned taken = 0;  // bit t: column lane + 32 t already chosen
     for (int m = 0; m < g.topk; ++m) {
