@@ -370,20 +370,21 @@ def our_arm(args, wl):
     route_ms = time_graphs(kernel_graphs(launch_route))
     attend_ms = time_graphs(kernel_graphs(launch_attend))
 
-    # end to end through the public API with pinned host buffers
-    hb = bra.HostBuffers(host[0].shape, tdt, wl.S, wl.topk, dev)
-    out_h = torch.empty(host[0].shape, dtype=tdt).pin_memory()
+    # end to end through the public API with pinned host buffers: copies in,
+    # forward and copies out of consecutive batches overlapped (HostPipeline)
+    pipe = bra.HostPipeline(host[0].shape, tdt, wl.S, wl.topk, dev)
+    outs_h = [torch.empty(host[0].shape, dtype=tdt).pin_memory() for _ in range(2)]
     es = max(1, args.e2e_steps)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            bra.forward_host(*host, wl.heads, wl.S, wl.topk, w, b, out_h, hb, stream=stream)
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(es):
-            bra.forward_host(*host, wl.heads, wl.S, wl.topk, w, b, out_h, hb, stream=stream)
-        e1.record(stream)
-        e1.synchronize()
+    for i in range(3):
+        pipe.submit(*host, wl.heads, wl.S, wl.topk, w, b, outs_h[i % 2])
+    pipe.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(pipe.copy_in)
+    for i in range(es):
+        pipe.submit(*host, wl.heads, wl.S, wl.topk, w, b, outs_h[i % 2])
+    e1.record(pipe.copy_out)
+    e1.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
         import torch.distributed as dist

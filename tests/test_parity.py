@@ -118,3 +118,21 @@ def test_side_stream_and_determinism(cuda_device):
     o2, i2 = bra.forward(q, k, v, wl.heads, wl.S, wl.topk, w, b)
     torch.cuda.synchronize()
     assert torch.equal(i1, i2) and torch.equal(o1, o2)
+
+
+def test_host_pipeline_matches_forward(cuda_device):
+    """Overlapped host batches give exactly the device forward's results."""
+    wl = bra_synth.WORKLOADS["stage2_bf16"].replace(B=2)
+    batches = [bra_synth.make_inputs(wl, seed=s) for s in (31, 32, 33)]
+    w = torch.from_numpy(batches[0].lepe_w).to(cuda_device)
+    b = torch.from_numpy(batches[0].lepe_b).to(cuda_device)
+    host = [[torch.from_numpy(a).to(torch.bfloat16).pin_memory() for a in (x.q, x.k, x.v)]
+            for x in batches]
+    outs = [torch.empty_like(h[0]).pin_memory() for h in host]
+    pipe = bra.HostPipeline(host[0][0].shape, torch.bfloat16, wl.S, wl.topk, cuda_device)
+    for h, o in zip(host, outs):
+        pipe.submit(*h, wl.heads, wl.S, wl.topk, w, b, o)
+    pipe.synchronize()
+    for h, o in zip(host, outs):
+        ref, _ = bra.forward(*(t.to(cuda_device) for t in h), wl.heads, wl.S, wl.topk, w, b)
+        assert torch.equal(o, ref.cpu())

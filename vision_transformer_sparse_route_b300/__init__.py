@@ -15,6 +15,7 @@ import os
 import torch
 
 __all__ = ["BraError", "route", "attend", "forward", "forward_static", "forward_host",
+           "HostPipeline",
            "idx_workspace_bytes", "device_status", "library_path", "SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -190,6 +191,55 @@ def forward_host(q, k, v, heads: int, S: int, topk: int, lepe_w, lepe_b, out,
                 out=buffers.out, idx=buffers.idx, stream=s)
         out.copy_(buffers.out, non_blocking=True)
     return out
+
+
+class HostPipeline:
+    """BRA forwards on host tensors with copies and compute overlapped.
+
+    Each `submit` copies one batch's q, k, v (pinned host tensors) to a device
+    buffer set on a copy-in stream, runs bra_forward on a compute stream once
+    they have landed, and copies out back on a copy-out stream. With `depth`
+    buffer sets, batch i's compute overlaps batch i+1's copy-in and batch
+    i-1's copy-out (the two copy directions use separate copy engines).
+    Submissions return at once; `synchronize` waits for all of them. The host
+    tensors passed to a submission must not change until it has completed.
+    """
+
+    def __init__(self, shape, dtype, S: int, topk: int, device, depth: int = 2):
+        self.slots = [HostBuffers(shape, dtype, S, topk, device) for _ in range(depth)]
+        self.copy_in = torch.cuda.Stream(device=device)
+        self.compute = torch.cuda.Stream(device=device)
+        self.copy_out = torch.cuda.Stream(device=device)
+        self._free = [None] * depth  # copy-out of the slot's last batch done
+        self._n = 0
+
+    def submit(self, q, k, v, heads: int, S: int, topk: int, lepe_w, lepe_b, out):
+        slot = self._n % len(self.slots)
+        buf = self.slots[slot]
+        if self._free[slot] is not None:
+            self.copy_in.wait_event(self._free[slot])
+        with torch.cuda.stream(self.copy_in):
+            buf.q.copy_(q, non_blocking=True)
+            buf.k.copy_(k, non_blocking=True)
+            buf.v.copy_(v, non_blocking=True)
+            landed = torch.cuda.Event()
+            landed.record(self.copy_in)
+        self.compute.wait_event(landed)
+        forward(buf.q, buf.k, buf.v, heads, S, topk, lepe_w, lepe_b, out=buf.out,
+                idx=buf.idx, stream=self.compute)
+        done = torch.cuda.Event()
+        done.record(self.compute)
+        self.copy_out.wait_event(done)
+        with torch.cuda.stream(self.copy_out):
+            out.copy_(buf.out, non_blocking=True)
+            freed = torch.cuda.Event()
+            freed.record(self.copy_out)
+        self._free[slot] = freed
+        self._n += 1
+        return out
+
+    def synchronize(self):
+        self.copy_out.synchronize()
 
 
 def device_status(stream=None, clear: bool = True) -> int:
