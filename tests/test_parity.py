@@ -3,7 +3,10 @@
 Small shapes span several tiles, ragged regions (slots padded to 8 rows),
 LePE borders, one region (dense attention), all regions routed and large
 region grids; the full-size workloads run at the sizes the benchmark times,
-with every output compared against the oracle.
+with every output compared against the oracle. Maps whose regions hold fewer
+than 16 tokens and whose 64-channel chunk fits in shared memory take the
+image-resident attend kernel (the image_* and n4 / ragged_n15 shapes); the
+others take the region kernel.
 """
 import numpy as np
 import pytest
@@ -29,6 +32,11 @@ SMALL = [
     Workload("tall_region_bf16", 1, 40, 8, 64, 2, 4, 3, 5, "bf16"),
     Workload("grid32_bf16", 1, 64, 64, 64, 2, 32, 2, 5, "bf16"),
     Workload("n16_c128_bf16", 3, 28, 28, 128, 4, 7, 4, 5, "bf16"),
+    Workload("ragged_n15_region_bf16", 1, 36, 60, 64, 2, 12, 3, 5, "bf16"),
+    Workload("image_ks3_bf16", 3, 12, 12, 64, 2, 4, 5, 3, "bf16"),
+    Workload("image_ks7_bf16", 2, 14, 14, 128, 4, 7, 4, 7, "bf16"),
+    Workload("image_ks1_128keys_bf16", 2, 8, 16, 64, 2, 4, 16, 1, "bf16"),
+    Workload("image_wide_c256_bf16", 1, 6, 15, 256, 8, 3, 7, 5, "bf16"),
     Workload("small_f32", 2, 12, 12, 64, 2, 3, 3, 5, "f32"),
     Workload("ragged_f32", 1, 15, 10, 32, 1, 5, 4, 3, "f32"),
     Workload("d64_f32", 1, 8, 8, 128, 2, 2, 2, 5, "f32"),
@@ -74,22 +82,26 @@ def test_no_bias_and_repeated_routing(cuda_device):
     assert np.abs(out.float().cpu().numpy() - ref).max() <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_out_of_range_index_reads_zeros_and_flags(dtype, cuda_device):
-    wl = Workload("bad", 1, 16, 16, 64, 2, 2, 2, 3, dtype)
+@pytest.mark.parametrize("dtype,H,S", [("bf16", 16, 2), ("f32", 16, 2), ("bf16", 14, 7)],
+                         ids=["bf16_region", "f32", "bf16_image"])
+def test_out_of_range_index_reads_zeros_and_flags(dtype, H, S, cuda_device):
+    wl = Workload("bad", 1, H, H, 64, 2, S, 2, 3, dtype)
     x = bra_synth.make_inputs(wl, seed=2)
     q, k, v, w, b = device_inputs(wl, x, cuda_device)
-    idx = np.array([[[0, 1], [1, 9], [2, -1], [3, 0]]], dtype=np.int32)
+    R = S * S
+    good = np.stack([np.arange(R), (np.arange(R) + 1) % R], axis=1)[None].astype(np.int32)
+    idx = good.copy()
+    idx[0, 1:, 1] = np.where(np.arange(1, R) % 2, R + np.arange(1, R), -np.arange(1, R))
     bra.device_status(clear=True)
     out = bra.attend(q, k, v, torch.from_numpy(idx).to(cuda_device), wl.heads, wl.S, w, b)
     assert bra.device_status(clear=True) == bra.BRA_ERR_INVALID_ARG
     assert bra.device_status(clear=True) == bra.BRA_OK
     got = out.float().cpu().numpy()
     assert np.isfinite(got).all()
-    # rows whose routing is valid are unaffected
-    good = np.array([[[0, 1], [1, 0], [2, 0], [3, 0]]], dtype=np.int32)
+    # region 0, whose routing is valid, is unaffected
     ref = oracle.attend(x.q, x.k, x.v, good, wl.heads, wl.S, x.lepe_w, x.lepe_b)
-    assert np.abs(got[:, :8, :8] - ref[:, :8, :8]).max() <= TOL[dtype]
+    hr = H // S
+    assert np.abs(got[:, :hr, :hr] - ref[:, :hr, :hr]).max() <= TOL[dtype]
 
 
 def test_empty_batch_is_a_no_op(cuda_device):

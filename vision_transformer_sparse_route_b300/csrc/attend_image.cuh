@@ -1,0 +1,317 @@
+// attend_image.cuh -- routed attention + LePE for bf16 maps small enough that
+// one 64-channel chunk of a whole image's q, k and v fits in shared memory
+// (the stage-3 shape: 14 x 14 tokens, regions of 2 x 2).
+//
+// Same operation as attend_bf16.cuh (page "CVPR2023：BiFormer中的双层路由
+// 注意力机制解析" §3; LePE of page "从静态到动态：BRA双层路由注意力如何革新
+// 视觉Transformer的计算范式" §4), organised around the image instead of the
+// query region: regions of a few tokens make per-region copies tiny (a 2 x 2
+// region is 512 bytes per channel chunk), while the whole image chunk is a
+// handful of large box copies.
+//
+// One CTA per (image, 64-channel chunk). Four TMA box copies bring the chunk
+// of Q, K and V for the whole image (128-byte swizzled, one row per token)
+// and the V halo (image plus ks/2 border, zero filled). The routed keys are
+// gathered without copying: ldmatrix takes one row address per lane, so each
+// lane points at the token of the routed region it loads. Each warp then runs
+// (query region, head, 16 query rows) tasks with the same mma.sync attention
+// as the region kernel, O (f32) goes to shared memory, and every thread
+// computes the LePE of (channel pair, column, block of rows) items over the
+// whole image, adds O and stores bf16 to the output.
+#pragma once
+
+#include "attend_bf16.cuh"
+
+namespace bra {
+
+constexpr int kImgWarps = 16;
+constexpr int kImgThreads = 32 * kImgWarps;
+
+struct ImageGeom {
+  int H, W, C, S, heads, topk;
+  int hr, wr, n, R;
+  int nc;            // 64-channel chunks
+  int nkeys;         // topk * n keys per query
+  int q_blocks;      // 16-row query blocks per region
+  int halo_w, halo_h;
+  uint32_t tile;     // bytes of one [H*W + 1][128 B] tile (the last row stays
+                     // zero), rounded to 1024
+  uint32_t off_k, off_v, off_h, off_o, off_w, off_idx, off_bar;
+  float scale_log2;  // d^-1/2 * log2(e)
+};
+
+// Image token of key `key` of query region i: routed region key / n (from the
+// staged routing row ri), token key % n of it. Keys past nkeys (their logits
+// are masked) and keys of an out-of-range routed region (staged as -1) map to
+// the zero row after the image's tokens, so the latter read zeros.
+__device__ __forceinline__ int key_token(const ImageGeom &g, const int32_t *ri, int key) {
+  if (key >= g.nkeys) return g.H * g.W;
+  const int m = key / g.n, t = key - m * g.n;
+  const int j = ri[m];
+  if (j < 0) return g.H * g.W;
+  const int ty = t / g.wr, tx = t - ty * g.wr;
+  return ((j / g.S) * g.hr + ty) * g.W + (j % g.S) * g.wr + tx;
+}
+
+// Byte offset of 16-byte chunk `chunk` of token row `tok` in a swizzled tile.
+__device__ __forceinline__ uint32_t tok_addr(int tok, int chunk) {
+  return static_cast<uint32_t>(tok * 128 + ((chunk ^ (tok & 7)) << 4));
+}
+
+// One attention task: query rows qb*16 .. +15 of region i, head hl of the
+// chunk. Leaves the normalised O rows (row0 = qb*16 + lane/4 and row0 + 8,
+// channels hl*32 + a*8 + 2*(lane%4)) in o.
+template <bool MASKED>
+__device__ __forceinline__ void image_attention_task(const ImageGeom &g, int i, int hl,
+                                                     int qb, uint32_t q_base,
+                                                     uint32_t k_base, uint32_t v_base,
+                                                     const int32_t *ri, float (&o)[4][4],
+                                                     int lane) {
+  const int cb = hl * 4;  // first 16-byte chunk of the head in the 128-byte row
+  const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
+  uint32_t qa[2][4];
+  {
+    int r = qb * 16 + (lane & 15);
+    r = r < g.n ? r : 0;  // rows past the region repeat its first token
+    const int tok = (y0 + r / g.wr) * g.W + x0 + r % g.wr;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+      ldsm_x4(q_base + tok_addr(tok, cb + ks * 2 + (lane >> 4)), qa[ks][0], qa[ks][1],
+              qa[ks][2], qa[ks][3]);
+  }
+  float l4[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    l4[a] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[a][e] = 0.f;
+  }
+  float m_run[2] = {-INFINITY, -INFINITY};
+  const uint32_t ones = 0x3f803f80u;  // two bf16 1.0
+  const float2 sc2 = make_float2(g.scale_log2, g.scale_log2);
+
+  for (int kb = 0; kb < g.nkeys; kb += 64) {
+    float s[8][4];
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[jt][e] = 0.f;
+      const int tok = key_token(g, ri, kb + jt * 8 + (lane & 7));
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(k_base + tok_addr(tok, cb + (lane >> 3)), b0, b1, b2, b3);
+      mma_bf16_16816(s[jt], qa[0], b0, b1);
+      mma_bf16_16816(s[jt], qa[1], b2, b3);
+    }
+    if (MASKED) {
+#pragma unroll
+      for (int jt = 0; jt < 8; ++jt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (kb + jt * 8 + 2 * (lane & 3) + (e & 1) >= g.nkeys) s[jt][e] = -INFINITY;
+    }
+    float mx[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float m = max3(s[0][2 * r], s[0][2 * r + 1], s[1][2 * r]);
+      m = max3(m, s[1][2 * r + 1], s[2][2 * r]);
+      m = max3(m, s[2][2 * r + 1], s[3][2 * r]);
+      m = max3(m, s[3][2 * r + 1], s[4][2 * r]);
+      m = max3(m, s[4][2 * r + 1], s[5][2 * r]);
+      m = max3(m, s[5][2 * r + 1], s[6][2 * r]);
+      m = max3(m, s[6][2 * r + 1], s[7][2 * r]);
+      m = fmaxf(m, s[7][2 * r + 1]);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      mx[r] = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    }
+    float2 nb[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float m_new = fmaxf(m_run[r], mx[r] * g.scale_log2);
+      const float base = (m_new == -INFINITY) ? 0.f : m_new;
+      if (kb > 0) {
+        const float alpha = exp2f(m_run[r] - base);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          o[a][2 * r] *= alpha;
+          o[a][2 * r + 1] *= alpha;
+        }
+        l4[2 * r] *= alpha;
+        l4[2 * r + 1] *= alpha;
+      }
+      m_run[r] = m_new;
+      nb[r] = make_float2(-base, -base);
+    }
+    uint32_t p[8][2];
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) {
+      const float2 x0v = __ffma2_rn(make_float2(s[jt][0], s[jt][1]), sc2, nb[0]);
+      const float2 x1v = __ffma2_rn(make_float2(s[jt][2], s[jt][3]), sc2, nb[1]);
+      p[jt][0] = exp2_bf16x2(x0v.x, x0v.y);
+      p[jt][1] = exp2_bf16x2(x1v.x, x1v.y);
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t pa[4] = {p[2 * t][0], p[2 * t][1], p[2 * t + 1][0], p[2 * t + 1][1]};
+      const int tok = key_token(g, ri, kb + t * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_trans(v_base + tok_addr(tok, cb + (lane >> 4)), r0, r1, r2, r3);
+      mma_bf16_16816(o[0], pa, r0, r1);
+      mma_bf16_16816(o[1], pa, r2, r3);
+      ldsm_x4_trans(v_base + tok_addr(tok, cb + 2 + (lane >> 4)), r0, r1, r2, r3);
+      mma_bf16_16816(o[2], pa, r0, r1);
+      mma_bf16_16816(o[3], pa, r2, r3);
+      mma_bf16_16816(l4, pa, ones, ones);  // row sums of the bf16 P
+    }
+  }
+  const float inv0 = 1.f / l4[0], inv1 = 1.f / l4[2];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    o[a][0] *= inv0; o[a][1] *= inv0;
+    o[a][2] *= inv1; o[a][3] *= inv1;
+  }
+}
+
+// LePE of image rows ry0 .. ry0+RB-1, column x, chunk channels c, c+1, plus O
+// from so ([H*W][64] f32, o_index layout), rounded to bf16 and stored to
+// gout (the image's first token at this chunk's first channel).
+template <int KS, int RB>
+__device__ __forceinline__ void image_lepe_item(const ImageGeom &g, const uint8_t *hb,
+                                                const float *so, __nv_bfloat16 *gout, int c,
+                                                int x, int ry0, const float *sw) {
+  float2 wgt[KS * KS];
+#pragma unroll
+  for (int e = 0; e < KS * KS; ++e) wgt[e] = *reinterpret_cast<const float2 *>(sw + e * 64 + c);
+  const float2 bias = *reinterpret_cast<const float2 *>(sw + KS * KS * 64 + c);
+  float2 acc[RB];
+#pragma unroll
+  for (int r = 0; r < RB; ++r) acc[r] = bias;
+  const uint8_t *col = hb + (ry0 * g.halo_w + x) * 128 + c * 2;
+#pragma unroll
+  for (int yy = 0; yy < RB + KS - 1; ++yy) {
+    if (ry0 + yy < g.halo_h) {
+      const uint8_t *rp = col + yy * g.halo_w * 128;
+#pragma unroll
+      for (int w = 0; w < KS; ++w) {
+        const uint32_t t2 = *reinterpret_cast<const uint32_t *>(rp + w * 128);
+        const float2 v = make_float2(__uint_as_float(__byte_perm(t2, 0u, 0x1044u)),
+                                     __uint_as_float(__byte_perm(t2, 0u, 0x3244u)));
+#pragma unroll
+        for (int u = 0; u < KS; ++u) {
+          const int r = yy - u;
+          if (r >= 0 && r < RB) acc[r] = __ffma2_rn(wgt[u * KS + w], v, acc[r]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < RB; ++r) {
+    const int row = ry0 + r;
+    if (row < g.H) {
+      const int t = row * g.W + x;
+      const float2 ov = *reinterpret_cast<const float2 *>(so + o_index(64, t, c));
+      const float2 sum = __fadd2_rn(acc[r], ov);
+      *reinterpret_cast<uint32_t *>(gout + (size_t)t * g.C + c) = pack_bf16x2(sum.x, sum.y);
+    }
+  }
+}
+
+template <int KS, int RB>
+__global__ void __launch_bounds__(kImgThreads, 1)
+    bra_attend_image_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_vh,
+                            __nv_bfloat16 *__restrict__ out,
+                            const int32_t *__restrict__ idx,
+                            const float *__restrict__ lepe_w,
+                            const float *__restrict__ lepe_b, ImageGeom g) {
+  extern __shared__ uint8_t image_smem_raw[];
+  uint8_t *smem = image_smem_raw + ((1024u - (smem_u32(image_smem_raw) & 1023u)) & 1023u);
+  float *so = reinterpret_cast<float *>(smem + g.off_o);    // [H*W][64]
+  float *sw = reinterpret_cast<float *>(smem + g.off_w);    // [KS*KS][64], bias [64]
+  int32_t *sidx = reinterpret_cast<int32_t *>(smem + g.off_idx);  // [R][topk]
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + g.off_bar);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x / g.nc, cc = blockIdx.x % g.nc;
+  constexpr int PAD = KS / 2;
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  // this chunk's LePE weights, tap-major
+  for (int e = tid; e < 64 * KS * KS; e += kImgThreads) {
+    const int tap = e / 64, c = e % 64;
+    sw[e] = __ldg(lepe_w + (size_t)(cc * 64 + c) * KS * KS + tap);
+  }
+  for (int c = tid; c < 64; c += kImgThreads)
+    sw[KS * KS * 64 + c] = lepe_b ? __ldg(lepe_b + cc * 64 + c) : 0.f;
+  // the zero row of K and V (no copy writes it)
+  if (tid < 16)
+    *reinterpret_cast<uint4 *>(smem + (tid < 8 ? g.off_k : g.off_v) + g.H * g.W * 128 +
+                               (tid & 7) * 16) = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, 3 * g.H * g.W * 128 + g.halo_w * g.halo_h * 128);
+    tma_load_4d(smem, &tm_q, bar, cc * 64, 0, 0, b);
+    tma_load_4d(smem + g.off_k, &tm_k, bar, cc * 64, 0, 0, b);
+    tma_load_4d(smem + g.off_v, &tm_v, bar, cc * 64, 0, 0, b);
+    tma_load_4d(smem + g.off_h, &tm_vh, bar, cc * 64, -PAD, -PAD, b);
+  }
+  // the image's routing, staged (it comes from the previous grid)
+  grid_dependency_wait();
+  for (int e = tid; e < g.R * g.topk; e += kImgThreads) {
+    int j = __ldg(idx + (size_t)b * g.R * g.topk + e);
+    if (j < 0 || j >= g.R) {  // out of range: its keys read zeros, flag it
+      atomicOr(&g_status, kStatusBadIndex);
+      j = -1;
+    }
+    sidx[e] = j;
+  }
+  __syncthreads();
+  mbar_wait(bar, 0);
+
+  // ---- attention: (query region, head of the chunk, query block) tasks
+  const uint32_t q_base = smem_u32(smem), k_base = smem_u32(smem + g.off_k),
+                 v_base = smem_u32(smem + g.off_v);
+  const int tasks = g.R * 2 * g.q_blocks;
+  for (int task = warp; task < tasks; task += kImgWarps) {
+    const int i = task / (2 * g.q_blocks), rest = task % (2 * g.q_blocks);
+    const int hl = rest % 2, qb = rest / 2;
+    float o[4][4];
+    if (g.nkeys % 64)
+      image_attention_task<true>(g, i, hl, qb, q_base, k_base, v_base, sidx + i * g.topk, o,
+                                 lane);
+    else
+      image_attention_task<false>(g, i, hl, qb, q_base, k_base, v_base, sidx + i * g.topk, o,
+                                  lane);
+    const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int r = qb * 16 + (lane >> 2) + half * 8;
+      if (r < g.n) {
+        const int tok = (y0 + r / g.wr) * g.W + x0 + r % g.wr;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int ch = hl * 32 + a * 8 + 2 * (lane & 3);
+          *reinterpret_cast<float2 *>(so + o_index(64, tok, ch)) =
+              make_float2(o[a][2 * half], o[a][2 * half + 1]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- LePE + O -> bf16 output
+  __nv_bfloat16 *gout = out + (size_t)b * g.H * g.W * g.C + cc * 64;
+  const uint8_t *hb = smem + g.off_h;
+  const int rblocks = (g.H + RB - 1) / RB;
+  for (int item = tid; item < 32 * g.W * rblocks; item += kImgThreads) {
+    const int cp = item % 32, rest = item / 32;
+    const int x = rest % g.W, ry0 = (rest / g.W) * RB;
+    image_lepe_item<KS, RB>(g, hb, so, gout, 2 * cp, x, ry0, sw);
+  }
+}
+
+}  // namespace bra

@@ -15,12 +15,14 @@
 #include "bra.h"
 #include "attend_bf16.cuh"
 #include "attend_f32.cuh"
+#include "attend_image.cuh"
 #include "route.cuh"
 
 namespace {
 
 using bra::AttendF32Geom;
 using bra::AttendGeom;
+using bra::ImageGeom;
 
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;
 
@@ -399,6 +401,38 @@ bool plan_attend_bf16(int B, int H, int W, int C, int heads, int S, int topk, in
   return *smem <= kMaxSmemPerBlock;
 }
 
+// The image-resident kernel: bf16, regions of fewer than 16 tokens (a 16-row
+// query block is then partly empty and a region's box copies are under 2 KB),
+// and one 64-channel chunk of the whole image's Q, K, V, V halo and f32 O in
+// shared memory.
+bool plan_attend_image(int H, int W, int C, int heads, int S, int topk, int ks,
+                       ImageGeom *g, size_t *smem) {
+  if (C % 64 || C / heads != 32) return false;
+  ImageGeom a = {};
+  a.H = H; a.W = W; a.C = C; a.S = S; a.heads = heads; a.topk = topk;
+  a.hr = H / S; a.wr = W / S; a.n = a.hr * a.wr; a.R = S * S;
+  if (a.n >= 16) return false;
+  a.halo_w = W + ks - 1;
+  a.halo_h = H + ks - 1;
+  if (a.halo_w > 256 || a.halo_h > 256) return false;  // TMA box limit
+  a.nc = C / 64;
+  a.nkeys = topk * a.n;
+  a.q_blocks = 1;
+  const size_t tokens = (size_t)H * W;
+  a.tile = (uint32_t)round_up((tokens + 1) * 128, 1024);
+  a.off_k = a.tile;
+  a.off_v = 2 * a.tile;
+  a.off_h = 3 * a.tile;
+  a.off_o = (uint32_t)round_up((size_t)a.off_h + (size_t)a.halo_w * a.halo_h * 128, 16);
+  a.off_w = (uint32_t)(a.off_o + tokens * 64 * 4);
+  a.off_idx = (uint32_t)(a.off_w + (size_t)(ks * ks + 1) * 64 * 4);
+  a.off_bar = (uint32_t)round_up((size_t)a.off_idx + (size_t)a.R * topk * 4, 8);
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
+  *smem = (size_t)a.off_bar + 8 + 1024;  // slack to align the base to 1024 bytes
+  *g = a;
+  return *smem <= kMaxSmemPerBlock;
+}
+
 bool plan_attend_f32(int H, int W, int C, int heads, int S, int topk, int ks,
                      AttendF32Geom *g, size_t *smem) {
   if (C % 4 || C / heads > 64) return false;
@@ -471,6 +505,45 @@ int launch_attend_bf16_ks(const void *q, const void *k, const void *v,
   }
 }
 
+template <int KS, int RB>
+int launch_attend_image_kr(const void *q, const void *k, const void *v,
+                           const int32_t *idx, int B, const float *w,
+                           const float *bias, void *out, const ImageGeom &g,
+                           size_t smem, bool pdl, cudaStream_t s) {
+  CUtensorMap tq, tk, tv, th;
+  if (!make_map(&tq, q, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map(&tk, k, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map(&tv, v, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map(&th, v, B, g.H, g.W, g.C, g.halo_w, g.halo_h, false))
+    return BRA_ERR_CUDA;
+  auto kern = bra::bra_attend_image_kernel<KS, RB>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((size_t)B * g.nc), 1, 1);
+  cfg.blockDim = dim3(bra::kImgThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, th,
+                                        static_cast<__nv_bfloat16 *>(out), idx, w, bias, g));
+}
+
+template <int KS>
+int launch_attend_image_ks(const void *q, const void *k, const void *v,
+                           const int32_t *idx, int B, const float *w,
+                           const float *bias, void *out, const ImageGeom &g,
+                           size_t smem, bool pdl, cudaStream_t s) {
+  // LePE row blocks: 7 rows when they tile the map exactly, else 8
+  if (g.H % 7 == 0)
+    return launch_attend_image_kr<KS, 7>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+  return launch_attend_image_kr<KS, 8>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+}
+
 template <int KS>
 int launch_attend_f32_ks(const void *q, const void *k, const void *v,
                          const int32_t *idx, int B, const float *w,
@@ -504,8 +577,11 @@ int check_attend(const void *q, const void *k, const void *v, const int32_t *idx
   if ((size_t)B * S * S > 0x7fffffffu) return BRA_ERR_UNSUPPORTED;
   size_t smem;
   if (dtype == BRA_BF16) {
+    ImageGeom gi;
     AttendGeom g;
-    if (!plan_attend_bf16(B, H, W, C, heads, S, topk, ks, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+    if (!plan_attend_image(H, W, C, heads, S, topk, ks, &gi, &smem) &&
+        !plan_attend_bf16(B, H, W, C, heads, S, topk, ks, &g, &smem))
+      return BRA_ERR_UNSUPPORTED;
   } else {
     AttendF32Geom g;
     if (!plan_attend_f32(H, W, C, heads, S, topk, ks, &g, &smem)) return BRA_ERR_UNSUPPORTED;
@@ -519,6 +595,15 @@ int launch_attend(const void *q, const void *k, const void *v, const int32_t *id
                   bool pdl, cudaStream_t s) {
   size_t smem;
   if (dtype == BRA_BF16) {
+    ImageGeom gi;
+    if (plan_attend_image(H, W, C, heads, S, topk, ks, &gi, &smem)) {
+      switch (ks) {
+        case 1: return launch_attend_image_ks<1>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+        case 3: return launch_attend_image_ks<3>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+        case 5: return launch_attend_image_ks<5>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+        default: return launch_attend_image_ks<7>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+      }
+    }
     AttendGeom g;
     plan_attend_bf16(B, H, W, C, heads, S, topk, ks, &g, &smem);
     switch (ks) {
