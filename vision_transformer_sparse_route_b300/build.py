@@ -13,7 +13,8 @@ LIB = os.path.join(PKG, "libbra.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 SOURCES = ["bra.cu"]
-DEPS = ["bra.cu", "ptx.cuh", "route.cuh", "attend_bf16.cuh", "attend_f32.cuh"]
+DEPS = ["bra.cu", "ptx.cuh", "route.cuh", "attend_bf16.cuh", "attend_f32.cuh",
+        "attend_image.cuh"]
 
 
 def nvcc_command(out: str, extra: list[str] | None = None) -> list[str]:

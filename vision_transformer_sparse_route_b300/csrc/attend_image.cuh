@@ -32,18 +32,20 @@ struct ImageGeom {
   int hr, wr, n, R;
   int nc;            // 64-channel chunks
   int nkeys;         // topk * n keys per query
+  int nkp;           // nkeys rounded up to 64 (key table row length)
   int q_blocks;      // 16-row query blocks per region
   int halo_w, halo_h;
   uint32_t tile;     // bytes of one [H*W + 1][128 B] tile (the last row stays
                      // zero), rounded to 1024
-  uint32_t off_k, off_v, off_h, off_o, off_w, off_idx, off_bar;
+  uint32_t off_k, off_v, off_h, off_o, off_w, off_idx, off_tab, off_bar;
   float scale_log2;  // d^-1/2 * log2(e)
 };
 
 // Image token of key `key` of query region i: routed region key / n (from the
 // staged routing row ri), token key % n of it. Keys past nkeys (their logits
 // are masked) and keys of an out-of-range routed region (staged as -1) map to
-// the zero row after the image's tokens, so the latter read zeros.
+// the zero row after the image's tokens, so the latter read zeros. Evaluated
+// once per (region, key) into the key table that the attention tasks read.
 __device__ __forceinline__ int key_token(const ImageGeom &g, const int32_t *ri, int key) {
   if (key >= g.nkeys) return g.H * g.W;
   const int m = key / g.n, t = key - m * g.n;
@@ -65,7 +67,7 @@ template <bool MASKED>
 __device__ __forceinline__ void image_attention_task(const ImageGeom &g, int i, int hl,
                                                      int qb, uint32_t q_base,
                                                      uint32_t k_base, uint32_t v_base,
-                                                     const int32_t *ri, float (&o)[4][4],
+                                                     const uint16_t *kt, float (&o)[4][4],
                                                      int lane) {
   const int cb = hl * 4;  // first 16-byte chunk of the head in the 128-byte row
   const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
@@ -96,7 +98,7 @@ __device__ __forceinline__ void image_attention_task(const ImageGeom &g, int i, 
     for (int jt = 0; jt < 8; ++jt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[jt][e] = 0.f;
-      const int tok = key_token(g, ri, kb + jt * 8 + (lane & 7));
+      const int tok = kt[kb + jt * 8 + (lane & 7)];
       uint32_t b0, b1, b2, b3;
       ldsm_x4(k_base + tok_addr(tok, cb + (lane >> 3)), b0, b1, b2, b3);
       mma_bf16_16816(s[jt], qa[0], b0, b1);
@@ -152,7 +154,7 @@ __device__ __forceinline__ void image_attention_task(const ImageGeom &g, int i, 
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const uint32_t pa[4] = {p[2 * t][0], p[2 * t][1], p[2 * t + 1][0], p[2 * t + 1][1]};
-      const int tok = key_token(g, ri, kb + t * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+      const int tok = kt[kb + t * 16 + (lane & 7) + ((lane >> 3) & 1) * 8];
       uint32_t r0, r1, r2, r3;
       ldsm_x4_trans(v_base + tok_addr(tok, cb + (lane >> 4)), r0, r1, r2, r3);
       mma_bf16_16816(o[0], pa, r0, r1);
@@ -230,6 +232,7 @@ __global__ void __launch_bounds__(kImgThreads, 1)
   float *so = reinterpret_cast<float *>(smem + g.off_o);    // [H*W][64]
   float *sw = reinterpret_cast<float *>(smem + g.off_w);    // [KS*KS][64], bias [64]
   int32_t *sidx = reinterpret_cast<int32_t *>(smem + g.off_idx);  // [R][topk]
+  uint16_t *ktab = reinterpret_cast<uint16_t *>(smem + g.off_tab);  // [R][nkp]
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + g.off_bar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -239,11 +242,16 @@ __global__ void __launch_bounds__(kImgThreads, 1)
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
+    mbar_arrive_expect_tx(bar, 3 * g.H * g.W * 128 + g.halo_w * g.halo_h * 128);
+    tma_load_4d(smem, &tm_q, bar, cc * 64, 0, 0, b);
+    tma_load_4d(smem + g.off_k, &tm_k, bar, cc * 64, 0, 0, b);
+    tma_load_4d(smem + g.off_v, &tm_v, bar, cc * 64, 0, 0, b);
+    tma_load_4d(smem + g.off_h, &tm_vh, bar, cc * 64, -PAD, -PAD, b);
   }
-  // this chunk's LePE weights, tap-major
+  // this chunk's LePE weights, read in their [c][tap] order, stored tap-major
   for (int e = tid; e < 64 * KS * KS; e += kImgThreads) {
-    const int tap = e / 64, c = e % 64;
-    sw[e] = __ldg(lepe_w + (size_t)(cc * 64 + c) * KS * KS + tap);
+    const int c = e / (KS * KS), tap = e - c * (KS * KS);
+    sw[tap * 64 + c] = __ldg(lepe_w + (size_t)cc * 64 * KS * KS + e);
   }
   for (int c = tid; c < 64; c += kImgThreads)
     sw[KS * KS * 64 + c] = lepe_b ? __ldg(lepe_b + cc * 64 + c) : 0.f;
@@ -252,13 +260,6 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     *reinterpret_cast<uint4 *>(smem + (tid < 8 ? g.off_k : g.off_v) + g.H * g.W * 128 +
                                (tid & 7) * 16) = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, 3 * g.H * g.W * 128 + g.halo_w * g.halo_h * 128);
-    tma_load_4d(smem, &tm_q, bar, cc * 64, 0, 0, b);
-    tma_load_4d(smem + g.off_k, &tm_k, bar, cc * 64, 0, 0, b);
-    tma_load_4d(smem + g.off_v, &tm_v, bar, cc * 64, 0, 0, b);
-    tma_load_4d(smem + g.off_h, &tm_vh, bar, cc * 64, -PAD, -PAD, b);
-  }
   // the image's routing, staged (it comes from the previous grid)
   grid_dependency_wait();
   for (int e = tid; e < g.R * g.topk; e += kImgThreads) {
@@ -268,6 +269,11 @@ __global__ void __launch_bounds__(kImgThreads, 1)
       j = -1;
     }
     sidx[e] = j;
+  }
+  __syncthreads();
+  for (int e = tid; e < g.R * g.nkp; e += kImgThreads) {
+    const int i = e / g.nkp;
+    ktab[e] = static_cast<uint16_t>(key_token(g, sidx + i * g.topk, e - i * g.nkp));
   }
   __syncthreads();
   mbar_wait(bar, 0);
@@ -281,10 +287,10 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     const int hl = rest % 2, qb = rest / 2;
     float o[4][4];
     if (g.nkeys % 64)
-      image_attention_task<true>(g, i, hl, qb, q_base, k_base, v_base, sidx + i * g.topk, o,
+      image_attention_task<true>(g, i, hl, qb, q_base, k_base, v_base, ktab + i * g.nkp, o,
                                  lane);
     else
-      image_attention_task<false>(g, i, hl, qb, q_base, k_base, v_base, sidx + i * g.topk, o,
+      image_attention_task<false>(g, i, hl, qb, q_base, k_base, v_base, ktab + i * g.nkp, o,
                                   lane);
     const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
 #pragma unroll

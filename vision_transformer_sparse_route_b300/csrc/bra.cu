@@ -286,16 +286,33 @@ bool wide_clusters_ok(int dtype, size_t smem) {
   return ok;
 }
 
-// Cluster size: 8 CTAs per image, 16 when the batch is too small to fill the
-// GPU with 8-CTA clusters and the device allows clusters of 16.
+// Route CTAs of a cluster size that one SM holds at once: limited by threads,
+// by the 64 registers a thread of the many-cluster shape and by shared memory
+// (228 KB an SM, 1 KB of it reserved per CTA).
+int route_ctas_per_sm(int B, int CL, size_t smem) {
+  const int nt = route_threads(B, CL);
+  const int by_smem = (int)(233472 / (smem + 1024));
+  return std::min(std::min(2048 / nt, 65536 / (64 * nt)), by_smem);
+}
+
+// Cluster size: 16 when the batch is too small to fill the GPU with 8-CTA
+// clusters and the device allows clusters of 16; otherwise the largest of 8,
+// 4 and 2 CTAs per image whose whole grid is resident at once (the copy of all
+// K means grows with C and limits CTAs per SM), else 8.
 int route_cluster(int B, int R, int H, int W, int C, int S, int topk, int dtype) {
   const int CL = std::min(8, R);
-  if (R < 16 || B * 8 >= sm_count()) return CL;
   bra::RouteGeom g;
   size_t smem;
   bool lk;
-  if (!plan_route(B, H, W, C, S, topk, dtype, 16, &g, &smem, &lk)) return CL;
-  return wide_clusters_ok(dtype, smem) ? 16 : CL;
+  if (R >= 16 && B * 8 < sm_count()) {
+    if (!plan_route(B, H, W, C, S, topk, dtype, 16, &g, &smem, &lk)) return CL;
+    return wide_clusters_ok(dtype, smem) ? 16 : CL;
+  }
+  for (int cl = CL; cl >= 2; cl /= 2) {
+    if (!plan_route(B, H, W, C, S, topk, dtype, cl, &g, &smem, &lk)) break;
+    if ((long long)B * cl <= (long long)route_ctas_per_sm(B, cl, smem) * sm_count()) return cl;
+  }
+  return CL;
 }
 
 int check_route(const void *q, const void *k, int B, int H, int W, int C, int S,
@@ -426,7 +443,9 @@ bool plan_attend_image(int H, int W, int C, int heads, int S, int topk, int ks,
   a.off_o = (uint32_t)round_up((size_t)a.off_h + (size_t)a.halo_w * a.halo_h * 128, 16);
   a.off_w = (uint32_t)(a.off_o + tokens * 64 * 4);
   a.off_idx = (uint32_t)(a.off_w + (size_t)(ks * ks + 1) * 64 * 4);
-  a.off_bar = (uint32_t)round_up((size_t)a.off_idx + (size_t)a.R * topk * 4, 8);
+  a.nkp = (int)round_up((size_t)a.nkeys, 64);
+  a.off_tab = (uint32_t)round_up((size_t)a.off_idx + (size_t)a.R * topk * 4, 16);
+  a.off_bar = (uint32_t)round_up((size_t)a.off_tab + (size_t)a.R * a.nkp * 2, 8);
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
   *smem = (size_t)a.off_bar + 8 + 1024;  // slack to align the base to 1024 bytes
   *g = a;
