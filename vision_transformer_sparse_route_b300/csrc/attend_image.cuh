@@ -37,23 +37,9 @@ struct ImageGeom {
   int halo_w, halo_h;
   uint32_t tile;     // bytes of one [H*W + 1][128 B] tile (the last row stays
                      // zero), rounded to 1024
-  uint32_t off_k, off_v, off_h, off_o, off_w, off_idx, off_tab, off_bar;
+  uint32_t off_k, off_v, off_h, off_o, off_w, off_tab, off_bar;
   float scale_log2;  // d^-1/2 * log2(e)
 };
-
-// Image token of key `key` of query region i: routed region key / n (from the
-// staged routing row ri), token key % n of it. Keys past nkeys (their logits
-// are masked) and keys of an out-of-range routed region (staged as -1) map to
-// the zero row after the image's tokens, so the latter read zeros. Evaluated
-// once per (region, key) into the key table that the attention tasks read.
-__device__ __forceinline__ int key_token(const ImageGeom &g, const int32_t *ri, int key) {
-  if (key >= g.nkeys) return g.H * g.W;
-  const int m = key / g.n, t = key - m * g.n;
-  const int j = ri[m];
-  if (j < 0) return g.H * g.W;
-  const int ty = t / g.wr, tx = t - ty * g.wr;
-  return ((j / g.S) * g.hr + ty) * g.W + (j % g.S) * g.wr + tx;
-}
 
 // Byte offset of 16-byte chunk `chunk` of token row `tok` in a swizzled tile.
 __device__ __forceinline__ uint32_t tok_addr(int tok, int chunk) {
@@ -231,7 +217,7 @@ __global__ void __launch_bounds__(kImgThreads, 1)
   uint8_t *smem = image_smem_raw + ((1024u - (smem_u32(image_smem_raw) & 1023u)) & 1023u);
   float *so = reinterpret_cast<float *>(smem + g.off_o);    // [H*W][64]
   float *sw = reinterpret_cast<float *>(smem + g.off_w);    // [KS*KS][64], bias [64]
-  int32_t *sidx = reinterpret_cast<int32_t *>(smem + g.off_idx);  // [R][topk]
+  // key table: image token of key `key` of query region i at [i][key]
   uint16_t *ktab = reinterpret_cast<uint16_t *>(smem + g.off_tab);  // [R][nkp]
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + g.off_bar);
 
@@ -248,32 +234,55 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     tma_load_4d(smem + g.off_v, &tm_v, bar, cc * 64, 0, 0, b);
     tma_load_4d(smem + g.off_h, &tm_vh, bar, cc * 64, -PAD, -PAD, b);
   }
-  // this chunk's LePE weights, read in their [c][tap] order, stored tap-major
-  for (int e = tid; e < 64 * KS * KS; e += kImgThreads) {
-    const int c = e / (KS * KS), tap = e - c * (KS * KS);
-    sw[tap * 64 + c] = __ldg(lepe_w + (size_t)cc * 64 * KS * KS + e);
+  // this chunk's LePE weights, read in their [c][tap] order (every load
+  // issued before the first store), stored tap-major
+  constexpr int NW = (64 * KS * KS + kImgThreads - 1) / kImgThreads;
+  float wv[NW];
+#pragma unroll
+  for (int u = 0; u < NW; ++u) {
+    const int e = tid + u * kImgThreads;
+    wv[u] = e < 64 * KS * KS ? __ldg(lepe_w + (size_t)cc * 64 * KS * KS + e) : 0.f;
   }
-  for (int c = tid; c < 64; c += kImgThreads)
-    sw[KS * KS * 64 + c] = lepe_b ? __ldg(lepe_b + cc * 64 + c) : 0.f;
+  const float bv = (tid < 64 && lepe_b) ? __ldg(lepe_b + cc * 64 + tid) : 0.f;
+#pragma unroll
+  for (int u = 0; u < NW; ++u) {
+    const int e = tid + u * kImgThreads;
+    if (e < 64 * KS * KS) {
+      const int c = e / (KS * KS), tap = e - c * (KS * KS);
+      sw[tap * 64 + c] = wv[u];
+    }
+  }
+  if (tid < 64) sw[KS * KS * 64 + tid] = bv;
   // the zero row of K and V (no copy writes it)
   if (tid < 16)
     *reinterpret_cast<uint4 *>(smem + (tid < 8 ? g.off_k : g.off_v) + g.H * g.W * 128 +
                                (tid & 7) * 16) = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-  // the image's routing, staged (it comes from the previous grid)
+  // The key table, one (query region i, routed slot m) at a time: keys
+  // m*n .. m*n+n-1 of region i are the tokens of routed region idx[b, i, m]
+  // in row-major order. An out-of-range region's keys and the keys past nkeys
+  // (masked) read the zero row after the image's tokens. The routing comes
+  // from the previous grid.
   grid_dependency_wait();
-  for (int e = tid; e < g.R * g.topk; e += kImgThreads) {
-    int j = __ldg(idx + (size_t)b * g.R * g.topk + e);
-    if (j < 0 || j >= g.R) {  // out of range: its keys read zeros, flag it
+  const int slots = g.R * g.topk;
+  const uint16_t zero_row = static_cast<uint16_t>(g.H * g.W);
+  for (int e = tid; e < slots; e += kImgThreads) {
+    const int i = e / g.topk, m = e - i * g.topk;
+    const int j = __ldg(idx + (size_t)b * slots + e);
+    uint16_t *row = ktab + i * g.nkp + m * g.n;
+    if (j < 0 || j >= g.R) {  // out of range: flag it
       atomicOr(&g_status, kStatusBadIndex);
-      j = -1;
+      for (int t = 0; t < g.n; ++t) row[t] = zero_row;
+    } else {
+      const int y0 = (j / g.S) * g.hr, x0 = (j % g.S) * g.wr;
+      for (int ty = 0; ty < g.hr; ++ty)
+        for (int tx = 0; tx < g.wr; ++tx)
+          row[ty * g.wr + tx] = static_cast<uint16_t>((y0 + ty) * g.W + x0 + tx);
     }
-    sidx[e] = j;
   }
-  __syncthreads();
-  for (int e = tid; e < g.R * g.nkp; e += kImgThreads) {
-    const int i = e / g.nkp;
-    ktab[e] = static_cast<uint16_t>(key_token(g, sidx + i * g.topk, e - i * g.nkp));
+  const int tail = g.nkp - g.nkeys;
+  for (int e = tid; e < g.R * tail; e += kImgThreads) {
+    const int i = e / tail;
+    ktab[i * g.nkp + g.nkeys + (e - i * tail)] = zero_row;
   }
   __syncthreads();
   mbar_wait(bar, 0);

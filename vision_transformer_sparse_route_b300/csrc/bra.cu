@@ -442,9 +442,8 @@ bool plan_attend_image(int H, int W, int C, int heads, int S, int topk, int ks,
   a.off_h = 3 * a.tile;
   a.off_o = (uint32_t)round_up((size_t)a.off_h + (size_t)a.halo_w * a.halo_h * 128, 16);
   a.off_w = (uint32_t)(a.off_o + tokens * 64 * 4);
-  a.off_idx = (uint32_t)(a.off_w + (size_t)(ks * ks + 1) * 64 * 4);
   a.nkp = (int)round_up((size_t)a.nkeys, 64);
-  a.off_tab = (uint32_t)round_up((size_t)a.off_idx + (size_t)a.R * topk * 4, 16);
+  a.off_tab = (uint32_t)round_up((size_t)a.off_w + (size_t)(ks * ks + 1) * 64 * 4, 16);
   a.off_bar = (uint32_t)round_up((size_t)a.off_tab + (size_t)a.R * a.nkp * 2, 8);
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
   *smem = (size_t)a.off_bar + 8 + 1024;  // slack to align the base to 1024 bytes
