@@ -90,7 +90,10 @@ int bra_route(const void *q, const void *k, int B, int H, int W, int C, int S,
  *   out       [B, H, W, C] device, dtype of q
  * Supported: bf16 with C % 64 == 0 and d == 32; f32 with C % 4 == 0 and
  * d <= 64; shared-memory footprint within the per-block limit. Otherwise
- * BRA_ERR_UNSUPPORTED.
+ * BRA_ERR_UNSUPPORTED. bf16 maps whose regions hold fewer than 16 tokens and
+ * whose whole image fits in shared memory one 64-channel chunk at a time
+ * (about 250 tokens) run an image-resident kernel; the others a persistent
+ * kernel over query regions. The choice depends on the shape only.
  */
 int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
                int B, int H, int W, int C, int heads, int S, int topk,
