@@ -30,9 +30,12 @@
 //              depthwise stencil from the halo with packed f32x2 FMAs, plus
 //              O, rounded once to bf16 into
 //              the group's output staging tile;
-// then one thread refills the stage with the copies of the unit `stages`
-// iterations ahead (its routing read by the group's first warp while the
-// unit was computed) and sends the staging tile out with a TMA store.
+// then the group's first warp refills the stage with the copies of the unit
+// `stages` iterations ahead (its routing read by that warp while the unit was
+// computed; one lane per box, one instruction for all boxes), while its last
+// warp sends the staging tile out with a TMA store. A box copy holds up the
+// thread that issues it for a long time (about a microsecond per instruction
+// on the stage-1 shape), so each of these sits on a different warp.
 #pragma once
 
 #include "ptx.cuh"
@@ -313,9 +316,12 @@ __device__ __forceinline__ void load_pair_weights(const float *sw, int C, int c,
 // --------------------------------------------------------------- copies
 // Issues the TMA copies of unit u into stage st, completing on bar: the Q
 // tile, the K and V tiles of the unit's routed regions and the V halo. Run by
-// a whole warp; lane 0 issues. jl holds routed region number `lane` of the
-// unit (read ahead by the caller) for lane < topk; regions beyond 32 are read
-// from idx here.
+// a whole warp. jl holds routed region number `lane` of the unit (read ahead
+// by the caller) for lane < topk. When the unit has at most 32 boxes, lane l
+// computes the operands of box l and one instruction issues them all (a box
+// copy costs its issuing thread far more than the instruction, so boxes from
+// one thread go out one after another); otherwise lane 0 issues every box,
+// reading regions beyond 32 from idx.
 template <int KS>
 __device__ __forceinline__ void issue_unit(const AttendGeom &g, const CUtensorMap *tm_q,
                                            const CUtensorMap *tm_k, const CUtensorMap *tm_v,
@@ -325,8 +331,40 @@ __device__ __forceinline__ void issue_unit(const AttendGeom &g, const CUtensorMa
   constexpr int PAD = KS / 2;
   const int b = u / g.R, i = u % g.R;
   const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
+  if (lane == 0) mbar_arrive_expect_tx(bar, g.tx_bytes);
+  __syncwarp();
+  const int nbox = g.nc * (2 + 2 * g.topk);
+  if (nbox <= 32) {
+    // box l: chunk l % nc of Q (l / nc == 0), the halo (1), then K and V of
+    // routed region m alternately (2 + 2m, 3 + 2m)
+    const int cc = lane % g.nc, r = lane / g.nc;
+    const int m = r >= 2 ? min((r - 2) >> 1, g.topk - 1) : 0;
+    const int j = __shfl_sync(0xffffffffu, jl, m);
+    const CUtensorMap *map = tm_q;
+    uint8_t *dst = st + cc * g.q_chunk;
+    int cx = x0, cy = y0;
+    if (r == 1) {
+      map = tm_vh;
+      dst = st + g.off_h + cc * g.h_chunk;
+      cx = x0 - PAD;
+      cy = y0 - PAD;
+    } else if (r >= 2) {
+      const bool is_v = (r - 2) & 1;
+      map = is_v ? tm_v : tm_k;
+      dst = st + (is_v ? g.off_v : g.off_k) + cc * g.kv_chunk + m * g.slot * 128u;
+      if (j < 0 || j >= g.R) {  // out of range: read zeros, flag it
+        if (lane < nbox) atomicOr(&g_status, kStatusBadIndex);
+        cx = 0;
+        cy = g.H;  // a box wholly below the image is all fill (zeros)
+      } else {
+        cx = (j % g.S) * g.wr;
+        cy = (j / g.S) * g.hr;
+      }
+    }
+    if (lane < nbox) tma_load_4d(dst, map, bar, cc * 64, cx, cy, b);
+    return;
+  }
   if (lane == 0) {
-    mbar_arrive_expect_tx(bar, g.tx_bytes);
     for (int cc = 0; cc < g.nc; ++cc)
       tma_load_4d(st + cc * g.q_chunk, tm_q, bar, cc * 64, x0, y0, b);
   }
@@ -506,22 +544,20 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
     fence_async_shared();  // staging tile (generic writes) before the TMA store
     named_sync(bar_id, kGroupThreads);
 
-    if (gw == 0) {
-      // the stage is no longer read: refill it, then send the output out
-      if (un < g.units)
-        issue_unit<KS>(g, &tm_q, &tm_k, &tm_v, &tm_vh, idx, jl, st, &full[s], un, lane);
-      if (lane == 0) {
-        const int b = u / g.R, i = u % g.R;
-        const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
-        for (int cc = 0; cc < g.nc; ++cc)
-          tma_store_4d(&tm_o, ob + cc * g.o_chunk, cc * 64, x0, y0, b);
-        tma_store_commit();
-        // the group's other staging tile (written next) must have been read
-        tma_store_wait_read_n<1>();
-      }
+    // the stage is no longer read: the group's first warp refills it while
+    // its last warp sends the output out (lane cc: channel chunk cc)
+    if (gw == 0 && un < g.units)
+      issue_unit<KS>(g, &tm_q, &tm_k, &tm_v, &tm_vh, idx, jl, st, &full[s], un, lane);
+    if (gw == kGroupWarps - 1 && lane < g.nc) {
+      const int b = u / g.R, i = u % g.R;
+      const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
+      tma_store_4d(&tm_o, ob + lane * g.o_chunk, lane * 64, x0, y0, b);
+      tma_store_commit();
+      // the group's other staging tile (written next) must have been read
+      tma_store_wait_read_n<1>();
     }
   }
-  if (grp < groups && gw == 0 && lane == 0) tma_store_wait_read();
+  if (grp < groups && gw == kGroupWarps - 1 && lane < g.nc) tma_store_wait_read();
 }
 
 }  // namespace bra
