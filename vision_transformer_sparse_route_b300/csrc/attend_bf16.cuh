@@ -61,6 +61,7 @@ struct AttendGeom {
   int stages;     // pipeline depth
   int masked;     // keys need masking (padded slots or a partial 64-key block)
   int alias;      // O overwrites the unit's Q/K/V once attention is done
+  int issue_warps;  // warps of a group that issue a refill's box copies
   int lepe_items; // (C / 2) * wr * ceil(hr / RB)
   uint32_t q_chunk, kv_chunk, h_chunk, o_chunk;  // bytes per chunk buffer
   uint32_t off_k, off_v, off_h;  // within a stage
@@ -316,28 +317,33 @@ __device__ __forceinline__ void load_pair_weights(const float *sw, int C, int c,
 // --------------------------------------------------------------- copies
 // Issues the TMA copies of unit u into stage st, completing on bar: the Q
 // tile, the K and V tiles of the unit's routed regions and the V halo. Run by
-// a whole warp. jl holds routed region number `lane` of the unit (read ahead
-// by the caller) for lane < topk. When the unit has at most 32 boxes, lane l
-// computes the operands of box l and one instruction issues them all (a box
+// warp `part` of nw warps. jl holds routed region number `lane` of the unit
+// (read ahead by the caller) for lane < topk. When the unit has at most 32 nw
+// boxes and at most 32 routed regions, lane l of warp `part` computes the
+// operands of box l nw + part and one instruction a warp issues them (a box
 // copy costs its issuing thread far more than the instruction, so boxes from
-// one thread go out one after another); otherwise lane 0 issues every box,
-// reading regions beyond 32 from idx.
+// one thread go out one after another); otherwise lane 0 of warp 0 issues
+// every box, reading regions beyond 32 from idx. Warp 0 posts the expected
+// byte count; copies of the other warps that complete before it only take
+// the barrier's transaction count below zero for a while, and the phase
+// cannot complete before warp 0's arrival.
 template <int KS>
 __device__ __forceinline__ void issue_unit(const AttendGeom &g, const CUtensorMap *tm_q,
                                            const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                            const CUtensorMap *tm_vh, const int32_t *idx,
                                            int jl, uint8_t *st, uint64_t *bar, int u,
-                                           int lane) {
+                                           int lane, int part = 0, int nw = 1) {
   constexpr int PAD = KS / 2;
   const int b = u / g.R, i = u % g.R;
   const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
-  if (lane == 0) mbar_arrive_expect_tx(bar, g.tx_bytes);
+  if (lane == 0 && part == 0) mbar_arrive_expect_tx(bar, g.tx_bytes);
   __syncwarp();
   const int nbox = g.nc * (2 + 2 * g.topk);
-  if (nbox <= 32) {
+  if (nbox <= 32 * nw && g.topk <= 32) {
+    const int l = lane * nw + part;
     // box l: chunk l % nc of Q (l / nc == 0), the halo (1), then K and V of
     // routed region m alternately (2 + 2m, 3 + 2m)
-    const int cc = lane % g.nc, r = lane / g.nc;
+    const int cc = l % g.nc, r = l / g.nc;
     const int m = r >= 2 ? min((r - 2) >> 1, g.topk - 1) : 0;
     const int j = __shfl_sync(0xffffffffu, jl, m);
     const CUtensorMap *map = tm_q;
@@ -353,7 +359,7 @@ __device__ __forceinline__ void issue_unit(const AttendGeom &g, const CUtensorMa
       map = is_v ? tm_v : tm_k;
       dst = st + (is_v ? g.off_v : g.off_k) + cc * g.kv_chunk + m * g.slot * 128u;
       if (j < 0 || j >= g.R) {  // out of range: read zeros, flag it
-        if (lane < nbox) atomicOr(&g_status, kStatusBadIndex);
+        if (l < nbox) atomicOr(&g_status, kStatusBadIndex);
         cx = 0;
         cy = g.H;  // a box wholly below the image is all fill (zeros)
       } else {
@@ -361,9 +367,10 @@ __device__ __forceinline__ void issue_unit(const AttendGeom &g, const CUtensorMa
         cy = (j / g.S) * g.hr;
       }
     }
-    if (lane < nbox) tma_load_4d(dst, map, bar, cc * 64, cx, cy, b);
+    if (l < nbox) tma_load_4d(dst, map, bar, cc * 64, cx, cy, b);
     return;
   }
+  if (part != 0) return;
   if (lane == 0) {
     for (int cc = 0; cc < g.nc; ++cc)
       tma_load_4d(st + cc * g.q_chunk, tm_q, bar, cc * 64, x0, y0, b);
@@ -489,7 +496,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
     const int s = it % g.stages;
     const int un = u + g.stages * gridDim.x;  // the unit this stage is refilled with
     int jl = 0;
-    if (gw == 0) {
+    if (gw < g.issue_warps) {
       grid_dependency_wait();
       if (un < g.units) jl = read_route_lane(g, idx, un, lane);  // lands while we work
     }
@@ -546,8 +553,8 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
 
     // the stage is no longer read: the group's first warp refills it while
     // its last warp sends the output out (lane cc: channel chunk cc)
-    if (gw == 0 && un < g.units)
-      issue_unit<KS>(g, &tm_q, &tm_k, &tm_v, &tm_vh, idx, jl, st, &full[s], un, lane);
+    if (gw < g.issue_warps && un < g.units)
+      issue_unit<KS>(g, &tm_q, &tm_k, &tm_v, &tm_vh, idx, jl, st, &full[s], un, lane, gw, g.issue_warps);
     if (gw == kGroupWarps - 1 && lane < g.nc) {
       const int b = u / g.R, i = u % g.R;
       const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;

@@ -401,6 +401,10 @@ bool plan_attend_bf16(int B, int H, int W, int C, int heads, int S, int topk, in
     a.stage_bytes = (uint32_t)round_up((size_t)a.off_o + o_bytes, 1024);
   }
   a.tx_bytes = a.nc * (a.o_chunk * (1u + 2u * topk) + a.h_chunk);
+  // about three box copies per issuing warp, at most four warps
+  const int nbox = a.nc * (2 + 2 * topk);
+  a.issue_warps = std::min(4, std::max(1, (nbox + 2) / 3));
+  if (topk > 32 || nbox > 32 * a.issue_warps) a.issue_warps = 1;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
   const size_t out_bytes = round_up((size_t)bra::kGroups * 2 * a.nc * a.o_chunk, 1024);
   const size_t w_bytes = round_up((size_t)(ks * ks + 1) * C * 4, 16);
