@@ -33,6 +33,7 @@ SMALL = [
     Workload("grid32_bf16", 1, 64, 64, 64, 2, 32, 2, 5, "bf16"),
     Workload("n16_c128_bf16", 3, 28, 28, 128, 4, 7, 4, 5, "bf16"),
     Workload("ragged_n15_region_bf16", 1, 36, 60, 64, 2, 12, 3, 5, "bf16"),
+    Workload("topk40_serial_copies_bf16", 1, 32, 32, 64, 2, 8, 40, 5, "bf16"),
     Workload("image_ks3_bf16", 3, 12, 12, 64, 2, 4, 5, 3, "bf16"),
     Workload("image_ks7_bf16", 2, 14, 14, 128, 4, 7, 4, 7, "bf16"),
     Workload("image_ks1_128keys_bf16", 2, 8, 16, 64, 2, 4, 16, 1, "bf16"),

@@ -159,6 +159,144 @@ __device__ __forceinline__ void image_attention_task(const ImageGeom &g, int i, 
   }
 }
 
+// The same attention in transposed form, for regions of at most 8 tokens,
+// both heads of the chunk at once (two independent MMA chains for the warp;
+// the key table lookups and token addresses are shared): the keys are the
+// MMA's 16 rows and the region's queries its 8 columns, so that half of each
+// MMA carries a query instead of a quarter. S^T = K Q^T; the softmax runs
+// down each column (a lane holds 8 of a column's 64 keys, three shuffles
+// combine them); movmatrix turns each 8x8 block of the bf16 P^T into the B
+// operand of O^T = V^T P^T; the column sums are an MMA of ones against the
+// same bf16 P^T. Leaves O^T of head h (channels h*32 + ct*16 + lane/4 and +8,
+// queries 2*(lane%4) and +1) in ot[h][ct][0..3] = (ch, q0), (ch, q1),
+// (ch+8, q0), (ch+8, q1).
+template <bool MASKED>
+__device__ __forceinline__ void image_attention_region_t(const ImageGeom &g, int i,
+                                                         uint32_t q_base, uint32_t k_base,
+                                                         uint32_t v_base, const uint16_t *kt,
+                                                         float (&ot)[2][2][4], int lane) {
+  const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
+  // Q^T as the B operand: one 8x8 block (queries x 8 channels) per chunk
+  uint32_t qb[2][2][2];
+  {
+    int r = lane & 7;
+    r = r < g.n ? r : 0;  // columns past the region repeat its first token
+    const int tok = (y0 + r / g.wr) * g.W + x0 + r % g.wr;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      ldsm_x4(q_base + tok_addr(tok, h * 4 + (lane >> 3)), qb[h][0][0], qb[h][0][1],
+              qb[h][1][0], qb[h][1][1]);
+  }
+  float l4[2][4];
+  float m_run[2][2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    m_run[h][0] = m_run[h][1] = -INFINITY;  // columns 2*(lane%4) and +1
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      l4[h][e] = 0.f;
+      ot[h][0][e] = 0.f;
+      ot[h][1][e] = 0.f;
+    }
+  }
+  const uint32_t ones[4] = {0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u};
+  const float2 sc2 = make_float2(g.scale_log2, g.scale_log2);
+  const int kr = (lane & 7) + ((lane >> 3) & 1) * 8;  // K block row of this lane
+  const int vr = (lane & 7) + (lane >> 4) * 8;        // V block row of this lane
+
+  for (int kb = 0; kb < g.nkeys; kb += 64) {
+    float s[2][4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int tok = kt[kb + mt * 16 + kr];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[h][mt][e] = 0.f;
+        uint32_t a[4];
+        ldsm_x4(k_base + tok_addr(tok, h * 4 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(s[h][mt], a, qb[h][0][0], qb[h][0][1]);
+        ldsm_x4(k_base + tok_addr(tok, h * 4 + 2 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(s[h][mt], a, qb[h][1][0], qb[h][1][1]);
+      }
+    }
+    if (MASKED) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (kb + mt * 16 + (lane >> 2) + (e >> 1) * 8 >= g.nkeys) s[h][mt][e] = -INFINITY;
+    }
+    float2 nb[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float m0 = max3(s[h][0][0], s[h][0][2], s[h][1][0]);
+      m0 = max3(m0, s[h][1][2], s[h][2][0]);
+      m0 = max3(m0, s[h][2][2], s[h][3][0]);
+      m0 = fmaxf(m0, s[h][3][2]);
+      float m1 = max3(s[h][0][1], s[h][0][3], s[h][1][1]);
+      m1 = max3(m1, s[h][1][3], s[h][2][1]);
+      m1 = max3(m1, s[h][2][3], s[h][3][1]);
+      m1 = fmaxf(m1, s[h][3][3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+      }
+      const float mx[2] = {m0, m1};
+      float base[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float m_new = fmaxf(m_run[h][q], mx[q] * g.scale_log2);
+        base[q] = (m_new == -INFINITY) ? 0.f : m_new;
+        if (kb > 0) {
+          const float alpha = exp2f(m_run[h][q] - base[q]);
+          ot[h][0][q] *= alpha;
+          ot[h][0][q + 2] *= alpha;
+          ot[h][1][q] *= alpha;
+          ot[h][1][q + 2] *= alpha;
+          l4[h][q] *= alpha;
+          l4[h][q + 2] *= alpha;
+        }
+        m_run[h][q] = m_new;
+      }
+      nb[h] = make_float2(-base[0], -base[1]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int tok = kt[kb + mt * 16 + vr];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // bf16 P^T rows g (keys mt*16 + g) and g + 8, columns q0, q1;
+        // transposed into the B fragments of keys 0-7 and 8-15 of this block
+        const float2 xt = __ffma2_rn(make_float2(s[h][mt][0], s[h][mt][1]), sc2, nb[h]);
+        const float2 xb = __ffma2_rn(make_float2(s[h][mt][2], s[h][mt][3]), sc2, nb[h]);
+        const uint32_t pb0 = movmatrix_trans(exp2_bf16x2(xt.x, xt.y));
+        const uint32_t pb1 = movmatrix_trans(exp2_bf16x2(xb.x, xb.y));
+#pragma unroll
+        for (int ct = 0; ct < 2; ++ct) {
+          uint32_t a[4];
+          ldsm_x4_trans(v_base + tok_addr(tok, h * 4 + ct * 2 + ((lane >> 3) & 1)), a[0], a[1],
+                        a[2], a[3]);
+          mma_bf16_16816(ot[h][ct], a, pb0, pb1);
+        }
+        mma_bf16_16816(l4[h], ones, pb0, pb1);  // column sums of the bf16 P^T
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float inv0 = 1.f / l4[h][0], inv1 = 1.f / l4[h][1];
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) {
+      ot[h][ct][0] *= inv0; ot[h][ct][1] *= inv1;
+      ot[h][ct][2] *= inv0; ot[h][ct][3] *= inv1;
+    }
+  }
+}
+
 // LePE of image rows ry0 .. ry0+RB-1, column x, chunk channels c, c+1, plus O
 // from so ([H*W][64] f32, o_index layout), rounded to bf16 and stored to
 // gout (the image's first token at this chunk's first channel).
@@ -244,6 +382,11 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     wv[u] = e < 64 * KS * KS ? __ldg(lepe_w + (size_t)cc * 64 * KS * KS + e) : 0.f;
   }
   const float bv = (tid < 64 && lepe_b) ? __ldg(lepe_b + cc * 64 + tid) : 0.f;
+  // the first routing entry of this thread (it comes from the previous grid),
+  // loaded before the weights are stored so that the two loads overlap
+  grid_dependency_wait();
+  const int slots = g.R * g.topk;
+  const int j0 = tid < slots ? __ldg(idx + (size_t)b * slots + tid) : 0;
 #pragma unroll
   for (int u = 0; u < NW; ++u) {
     const int e = tid + u * kImgThreads;
@@ -260,14 +403,11 @@ __global__ void __launch_bounds__(kImgThreads, 1)
   // The key table, one (query region i, routed slot m) at a time: keys
   // m*n .. m*n+n-1 of region i are the tokens of routed region idx[b, i, m]
   // in row-major order. An out-of-range region's keys and the keys past nkeys
-  // (masked) read the zero row after the image's tokens. The routing comes
-  // from the previous grid.
-  grid_dependency_wait();
-  const int slots = g.R * g.topk;
+  // (masked) read the zero row after the image's tokens.
   const uint16_t zero_row = static_cast<uint16_t>(g.H * g.W);
   for (int e = tid; e < slots; e += kImgThreads) {
     const int i = e / g.topk, m = e - i * g.topk;
-    const int j = __ldg(idx + (size_t)b * slots + e);
+    const int j = e == tid ? j0 : __ldg(idx + (size_t)b * slots + e);
     uint16_t *row = ktab + i * g.nkp + m * g.n;
     if (j < 0 || j >= g.R) {  // out of range: flag it
       atomicOr(&g_status, kStatusBadIndex);
@@ -290,10 +430,38 @@ __global__ void __launch_bounds__(kImgThreads, 1)
   // ---- attention: (query region, head of the chunk, query block) tasks
   const uint32_t q_base = smem_u32(smem), k_base = smem_u32(smem + g.off_k),
                  v_base = smem_u32(smem + g.off_v);
-  const int tasks = g.R * 2 * g.q_blocks;
+  if (g.n <= 8) {
+    // transposed form, one region (both heads of the chunk) per task
+    for (int i = warp; i < g.R; i += kImgWarps) {
+      float ot[2][2][4];
+      if (g.nkeys % 64)
+        image_attention_region_t<true>(g, i, q_base, k_base, v_base, ktab + i * g.nkp, ot, lane);
+      else
+        image_attention_region_t<false>(g, i, q_base, k_base, v_base, ktab + i * g.nkp, ot,
+                                        lane);
+      const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int r = 2 * (lane & 3) + e;  // query of column e
+        if (r < g.n) {
+          const int tok = (y0 + r / g.wr) * g.W + x0 + r % g.wr;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+              for (int half = 0; half < 2; ++half)
+                so[o_index(64, tok, h * 32 + ct * 16 + half * 8 + (lane >> 2))] =
+                    ot[h][ct][2 * half + e];
+        }
+      }
+    }
+  }
+  const int tasks = g.n <= 8 ? 0 : g.R * 2 * g.q_blocks;
   for (int task = warp; task < tasks; task += kImgWarps) {
     const int i = task / (2 * g.q_blocks), rest = task % (2 * g.q_blocks);
     const int hl = rest % 2, qb = rest / 2;
+    const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
     float o[4][4];
     if (g.nkeys % 64)
       image_attention_task<true>(g, i, hl, qb, q_base, k_base, v_base, ktab + i * g.nkp, o,
@@ -301,7 +469,6 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     else
       image_attention_task<false>(g, i, hl, qb, q_base, k_base, v_base, ktab + i * g.nkp, o,
                                   lane);
-    const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int r = qb * 16 + (lane >> 2) + half * 8;

@@ -146,6 +146,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0,
       : "r"(addr));
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held one row pair per lane
+// (lane l: row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1, low half first).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // D = A * B + D, m16n8k16, bf16 inputs, f32 accumulators.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4],
                                                const uint32_t (&a)[4],
