@@ -12,10 +12,13 @@
 // One CTA per (image, 64-channel chunk). Four TMA box copies bring the chunk
 // of Q, K and V for the whole image (128-byte swizzled, one row per token)
 // and the V halo (image plus ks/2 border, zero filled). The routed keys are
-// gathered without copying: ldmatrix takes one row address per lane, so each
-// lane points at the token of the routed region it loads. Each warp then runs
-// (query region, head, 16 query rows) tasks with the same mma.sync attention
-// as the region kernel, O (f32) goes to shared memory, and every thread
+// gathered without copying: a key table names the image token of every key
+// of every query region, and ldmatrix takes one row address per lane, so each
+// lane points at the token it loads. For regions of at most 8 tokens each
+// warp runs whole query regions (both heads of the chunk) in transposed form,
+// keys as the MMA's rows and queries as its columns; larger regions run
+// (query region, head, 16 query rows) tasks with the region kernel's
+// mma.sync attention. O (f32) goes to shared memory, and every thread then
 // computes the LePE of (channel pair, column, block of rows) items over the
 // whole image, adds O and stores bf16 to the output.
 #pragma once
