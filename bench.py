@@ -1,9 +1,12 @@
 #!/usr/bin/env python
 """BRA forward throughput on B300: tokens/s, roofline fraction, CPU oracle.
 
-One step is one BRA forward (bra_route + bra_attend through the C ABI) over
-one batch of the workload. Default workload: the BiFormer stage-1 shape
-(B=64, 56x56, C=64, 2 heads, S=7, top-1, LePE 5x5, bf16).
+One step is one BRA forward (bra_forward through the C ABI: routing, then
+routed attention + LePE) over one batch of the workload. The headline
+workload is the BiFormer stage-1 shape (B=64, 56x56, C=64, 2 heads, S=7,
+top-1, LePE 5x5, bf16); the line's `workloads` key measures all five
+workload shapes the same way (configs 1..5 in the order the workload
+statement lists them).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -39,23 +42,40 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 CSRC = os.path.join(ROOT, "vision_transformer_sparse_route_b300", "csrc")
 
+# Config numbers of the five workloads, in the order the workload statement
+# lists them.
+CONFIG_NUMBER = {"tiny_f32": 1, "stage1_bf16": 2, "stage2_bf16": 3, "stage3_bf16": 4,
+                 "seg512_bf16": 5}
 
-def parse_args():
+# Unit counts of a B300 SM for the ALU and MUFU ceilings: 128 float32 FMA
+# lanes (2 flops each) and 16 ex2 results per clock (the bf16x2 form returns
+# two exponentials per result).
+FP32_LANES_PER_SM = 128
+EX2_PER_SM_CLK = 16
+SM_FALLBACK, MHZ_FALLBACK = 148, 2032.0
+
+
+def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="stage1_bf16", choices=list(bra_synth.WORKLOADS))
+    p.add_argument("--workloads", default="all",
+                   help="workloads measured for the `workloads` key: all, none or a "
+                        "comma-separated list")
     p.add_argument("--sets", type=int, default=0, help="rotating input sets (0: auto)")
     p.add_argument("--e2e-steps", type=int, default=100)
     p.add_argument("--kernel-steps", type=int, default=200)
     p.add_argument("--load-seconds", type=float, default=1.5,
                    help="identical untimed steps before the timed region (clock samples)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--cpu-seconds-each", type=float, default=2.5,
+                   help="oracle seconds per (workload, thread count) of the `workloads` key")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-graph", action="store_true")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 # ----------------------------------------------------------------- helpers
@@ -81,6 +101,80 @@ def algorithmic_bytes(wl: bra_synth.Workload) -> dict:
     e = 4 if wl.dtype == "f32" else 2
     t = wl.B * wl.H * wl.W * wl.C * e
     return {"route": 2 * t, "attend": 4 * t, "forward": 4 * t}
+
+
+def algorithmic_work(wl: bra_synth.Workload) -> dict:
+    """Algorithmic work of each kernel and of the whole forward: bytes (inputs
+    read once, output written once), contraction flops of q k^T and p v,
+    other float32 flops (LePE 2 ks^2 per output element, affinity 2 R^2 C
+    and region pooling 2 N C per image) and exponentials (one per query and
+    routed key and head). The float32 path runs its contractions on the FMA
+    pipe, so there they count as ALU flops."""
+    N, R, n = wl.H * wl.W, wl.R, wl.n
+    b = algorithmic_bytes(wl)
+    contraction = 4 * wl.B * N * wl.topk * n * wl.C
+    lepe = 2 * wl.ks * wl.ks * wl.B * N * wl.C
+    affinity = 2 * wl.B * R * R * wl.C
+    pooling = 2 * wl.B * N * wl.C
+    exps = wl.B * N * wl.heads * wl.topk * n
+    tc = contraction if wl.dtype == "bf16" else 0
+    alu_c = 0 if wl.dtype == "bf16" else contraction
+    route = {"bytes": b["route"], "tensor_flops": 0, "alu_flops": affinity + pooling, "exps": 0}
+    attend = {"bytes": b["attend"], "tensor_flops": tc, "alu_flops": lepe + alu_c, "exps": exps}
+    fwd = {"bytes": b["forward"], "tensor_flops": tc,
+           "alu_flops": lepe + alu_c + affinity + pooling, "exps": exps}
+    return {"route": route, "attend": attend, "forward": fwd}
+
+
+def peaks(sm_count: int | None = None, sm_mhz: float | None = None) -> dict:
+    """Roofline denominators: HBM GB/s and bf16 tensor TFLOP/s measured on
+    the B300s (MEASURED_PEAKS.json, burst figures for kernels timed
+    alone), float32 ALU TFLOP/s and exponentials/s derived from the SM's unit
+    counts and its maximum clock."""
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        hbm, tc, kind = float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1800.0)), "measured"
+        mhz = sm_mhz or float(p.get("sm_max_mhz", MHZ_FALLBACK))
+    except (OSError, KeyError, ValueError):
+        hbm, tc, kind = 6400.0, 1800.0, "fallback"
+        mhz = sm_mhz or MHZ_FALLBACK
+    sms = sm_count or SM_FALLBACK
+    clk = mhz * 1e6
+    return {"hbm_gbs": hbm, "tensor_tflops": tc,
+            "alu_tflops": sms * FP32_LANES_PER_SM * 2 * clk / 1e12,
+            "ex2_per_s_f32": sms * EX2_PER_SM_CLK * clk,
+            "ex2_per_s_bf16": 2 * sms * EX2_PER_SM_CLK * clk,
+            "source": kind, "sm_count": sms, "sm_mhz": mhz}
+
+
+def measured_peaks():
+    p = peaks()
+    return p["hbm_gbs"], p["source"]
+
+
+def roofline(work: dict, pk: dict, dtype: str, seconds: float) -> dict:
+    """Roofline of one kernel (or the whole forward) that took `seconds`:
+    the slowest of bytes at HBM bandwidth, contraction flops at the tensor
+    peak, ALU flops at the float32 peak and exponentials at the MUFU rate;
+    `bound` names it, and achieved / peak are in its unit."""
+    ex2 = pk["ex2_per_s_bf16"] if dtype == "bf16" else pk["ex2_per_s_f32"]
+    terms = {
+        "hbm": (work["bytes"] / (pk["hbm_gbs"] * 1e9), work["bytes"] / 1e9, pk["hbm_gbs"],
+                "GB/s"),
+        "tensor": (work["tensor_flops"] / (pk["tensor_tflops"] * 1e12),
+                   work["tensor_flops"] / 1e12, pk["tensor_tflops"], "TFLOP/s"),
+        "alu": (work["alu_flops"] / (pk["alu_tflops"] * 1e12), work["alu_flops"] / 1e12,
+                pk["alu_tflops"], "TFLOP/s"),
+        "mufu": (work["exps"] / ex2, work["exps"] / 1e9, ex2 / 1e9, "G exp/s"),
+    }
+    bound = max(terms, key=lambda k: terms[k][0])
+    t_roof, amount, peak, unit = terms[bound]
+    achieved = amount / seconds if seconds > 0 else 0.0
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": t_roof / seconds if seconds > 0 else 0.0, "roof_us": t_roof * 1e6,
+            "measured_us": seconds * 1e6,
+            "terms_us": {k: v[0] * 1e6 for k, v in terms.items()}}
 
 
 class ClockSampler:
@@ -148,15 +242,6 @@ class ClockSampler:
                 "samples span the load phase before it)"}
 
 
-def measured_peaks():
-    try:
-        with open(PEAKS_FILE) as f:
-            p = json.load(f)
-        return p["hbm_gbs"], "measured"
-    except (OSError, KeyError, ValueError):
-        return 6400.0, "fallback"
-
-
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu capture, if it was taken on
     the current kernel sources; else None."""
@@ -169,6 +254,18 @@ def recorded_traffic(kernel: str, workload: str):
     if not e or e.get("sources") != sources_digest():
         return None
     return e.get("dram_bytes_per_launch")
+
+
+def selected_workloads(spec: str) -> list:
+    if spec in ("", "none"):
+        return []
+    if spec == "all":
+        return list(bra_synth.WORKLOADS)
+    names = [s.strip() for s in spec.split(",") if s.strip()]
+    for n in names:
+        if n not in bra_synth.WORKLOADS:
+            raise SystemExit(f"unknown workload {n}")
+    return names
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -229,6 +326,164 @@ def reference_arm(args, wl):
 
 
 # ------------------------------------------------------------------- ours
+class Setup:
+    """Device buffers, CUDA graphs and timers for one workload."""
+
+    def __init__(self, wl, dev, stream, x, sets_arg: int, use_graph: bool):
+        import torch
+        import vision_transformer_sparse_route_b300 as bra
+        self.torch, self.bra, self.wl, self.dev, self.stream = torch, bra, wl, dev, stream
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        self.tdt = tdt
+        cast = lambda a: torch.from_numpy(a).to(tdt)
+        self.host = [cast(a).pin_memory() for a in (x.q, x.k, x.v)]
+        self.w = torch.from_numpy(x.lepe_w).to(dev)
+        self.b = torch.from_numpy(x.lepe_b).to(dev)
+        ab = algorithmic_bytes(wl)
+        self.set_bytes = ab["forward"] + wl.B * wl.R * wl.topk * 4
+        self.sets = sets_arg or max(2, -(-3 * L2_BYTES // self.set_bytes) + 1)
+        self.bufs = []
+        for _ in range(self.sets):
+            q, k, v = (h.to(dev, non_blocking=True) for h in self.host)
+            out = torch.empty_like(q)
+            idx = torch.empty((wl.B, wl.R, wl.topk), dtype=torch.int32, device=dev)
+            self.bufs.append((q, k, v, out, idx))
+        torch.cuda.synchronize()
+        self.graphs = self.capture(self.fwd) if use_graph else []
+
+    def fwd(self, s):
+        q, k, v, out, idx = self.bufs[s % self.sets]
+        self.bra.forward(q, k, v, self.wl.heads, self.wl.S, self.wl.topk, self.w, self.b,
+                         out=out, idx=idx, stream=self.stream)
+
+    def route(self, s):
+        q, k, v, out, idx = self.bufs[s % self.sets]
+        self.bra.route(q, k, self.wl.S, self.wl.topk, idx=idx, stream=self.stream)
+
+    def attend(self, s):
+        q, k, v, out, idx = self.bufs[s % self.sets]
+        self.bra.attend(q, k, v, idx, self.wl.heads, self.wl.S, self.w, self.b, out=out,
+                        stream=self.stream)
+
+    def capture(self, launch):
+        """One CUDA graph per input set (launch overhead off the step)."""
+        torch = self.torch
+        gs = []
+        with torch.cuda.stream(self.stream):
+            for s in range(self.sets):
+                launch(s)  # warm the library (tensor-map entry point, attributes)
+            self.stream.synchronize()
+            for s in range(self.sets):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    launch(s)
+                gs.append(g)
+        torch.cuda.synchronize()
+        return gs
+
+    def step(self, i):
+        if self.graphs:
+            self.graphs[i % self.sets].replay()
+        else:
+            self.fwd(i)
+
+    def time_steps(self, n: int) -> float:
+        """ms for n forward steps, CUDA events on the launching stream."""
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for i in range(n):
+                self.step(i)
+            e1.record(self.stream)
+            e1.synchronize()
+        return e0.elapsed_time(e1)
+
+    def time_kernel(self, launch, steps: int) -> float:
+        """ms per launch of one kernel, replayed alone from its own CUDA graphs
+        over the rotating input sets."""
+        torch = self.torch
+        gs = self.capture(launch)
+        with torch.cuda.stream(self.stream):
+            for i in range(3):
+                gs[i % self.sets].replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for i in range(steps):
+                gs[i % self.sets].replay()
+            e1.record(self.stream)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    def release(self):
+        self.graphs = []
+        self.bufs = []
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+
+def launch_floor(torch, stream, reps: int = 2000) -> dict:
+    """Replay cost of a CUDA graph holding one near-empty kernel (a
+    one-element fill) and one holding two of them in a chain, back to back
+    on one stream: the floor under any one- or two-kernel forward."""
+    z = torch.zeros(1, device=stream.device)
+    out = {}
+    for nk in (1, 2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            z.fill_(0.0)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(nk):
+                    z.fill_(1.0)
+            for _ in range(10):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        out[f"graph_{nk}_kernel_us"] = e0.elapsed_time(e1) * 1e3 / reps
+    return out
+
+
+def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
+                     no_cpu: bool, use_graph: bool) -> dict:
+    """The `workloads` entry of one workload: forward ms/step, each kernel's
+    launch time, rooflines and the oracle at one thread and all cores."""
+    import torch
+    x = bra_synth.make_inputs(wl, seed=0)
+    st = Setup(wl, dev, stream, x, 0, use_graph)
+    for i in range(5):
+        st.step(i)
+    probe = st.time_steps(20) / 20
+    n = int(min(20000, max(200, 0.3 / max(probe * 1e-3, 1e-7))))
+    ms = st.time_steps(n) / n
+    route_ms = st.time_kernel(st.route, kernel_steps)
+    attend_ms = st.time_kernel(st.attend, kernel_steps)
+    work = algorithmic_work(wl)
+    ok = st.bra.device_status(stream)
+    st.release()
+    del st
+    entry = {"config": CONFIG_NUMBER.get(wl.name), "ms_per_step": ms, "steps_timed": n,
+             "tokens_per_s": wl.tokens / (ms * 1e-3), "route_us": route_ms * 1e3,
+             "attend_us": attend_ms * 1e3,
+             "step_roofline": roofline(work["forward"], pk, wl.dtype, ms * 1e-3),
+             "route_roofline": roofline(work["route"], pk, wl.dtype, route_ms * 1e-3),
+             "attend_roofline": roofline(work["attend"], pk, wl.dtype, attend_ms * 1e-3),
+             "device_status": ok}
+    if not no_cpu:
+        cores = os.cpu_count() or 1
+        v1, i1, _ = time_oracle(wl, x, cpu_seconds, 1)
+        va, ia, _ = time_oracle(wl, x, cpu_seconds, cores)
+        entry["oracle_tokens_per_s"] = {"threads_1": v1, f"threads_{cores}": va,
+                                        "images_sampled": [i1, ia], "cores": cores}
+    del x
+    torch.cuda.empty_cache()
+    return entry
+
+
 def our_arm(args, wl):
     import torch
     import vision_transformer_sparse_route_b300 as bra
@@ -240,51 +495,14 @@ def our_arm(args, wl):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    pk = peaks(props.multi_processor_count)
 
     # this rank's shard of a world * B image batch (weak scaling)
     wl_global = wl.replace(B=wl.B * world)
     x = bra_synth.make_inputs(wl_global, seed=0, batch=bra_synth.rank_slice(wl.B, rank))
-    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
-    cast = lambda a: torch.from_numpy(a).to(tdt)
-    host = [cast(a).pin_memory() for a in (x.q, x.k, x.v)]
-    w = torch.from_numpy(x.lepe_w).to(dev)
-    b = torch.from_numpy(x.lepe_b).to(dev)
-
-    ab = algorithmic_bytes(wl)
-    set_bytes = ab["forward"] + wl.B * wl.R * wl.topk * 4
-    sets = args.sets or max(2, -(-3 * L2_BYTES // set_bytes) + 1)
-    bufs = []
-    for s in range(sets):
-        q, k, v = (h.to(dev, non_blocking=True) for h in host)
-        out = torch.empty_like(q)
-        idx = torch.empty((wl.B, wl.R, wl.topk), dtype=torch.int32, device=dev)
-        bufs.append((q, k, v, out, idx))
-    torch.cuda.synchronize()
-
-    def fwd(s, stream=None):
-        q, k, v, out, idx = bufs[s % sets]
-        bra.forward(q, k, v, wl.heads, wl.S, wl.topk, w, b, out=out, idx=idx, stream=stream)
-
-    # one CUDA graph per input set (launch overhead off the step)
     stream = torch.cuda.Stream(device=dev)
-    graphs = []
-    if not args.no_graph:
-        with torch.cuda.stream(stream):
-            for s in range(sets):
-                fwd(s, stream)  # warm the library (tensor-map entry point, attributes)
-            stream.synchronize()
-            for s in range(sets):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    fwd(s, stream)
-                graphs.append(g)
-    torch.cuda.synchronize()
-
-    def step(i):
-        if graphs:
-            graphs[i % sets].replay()
-        else:
-            fwd(i, stream)
+    st = Setup(wl, dev, stream, x, args.sets, not args.no_graph)
 
     def barrier():
         torch.cuda.synchronize()
@@ -293,7 +511,6 @@ def our_arm(args, wl):
             dist.barrier()
         torch.cuda.synchronize()
 
-    props = torch.cuda.get_device_properties(dev)
     gpu_id = str(getattr(props, "uuid", "") or "")
     gpu_id = ("GPU-" + gpu_id) if gpu_id and not gpu_id.startswith("GPU-") else (gpu_id or "0")
     sampler = ClockSampler(gpu_id)
@@ -301,14 +518,14 @@ def our_arm(args, wl):
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            st.step(i)
         # untimed load phase: same steps, so clock samples reflect this load
         stream.synchronize()
         t_load = time.time()
         i = 0
         while time.time() - t_load < args.load_seconds:
             for _ in range(200):
-                step(i)
+                st.step(i)
                 i += 1
             stream.synchronize()
         barrier()
@@ -316,7 +533,7 @@ def our_arm(args, wl):
         t0 = time.time()
         ev0.record(stream)
         for i in range(args.steps):
-            step(i)
+            st.step(i)
         ev1.record(stream)
         ev1.synchronize()
         t1 = time.time()
@@ -333,56 +550,25 @@ def our_arm(args, wl):
     value = tokens / (ms / 1e3)
 
     # per-kernel durations: each kernel captured alone in a CUDA graph per input
-    # set and replayed back to back over the rotating sets (no host work between
-    # launches); CUDA events on the launching stream bracket the replays
+    # set and replayed back to back over the rotating sets
     ks = max(1, args.kernel_steps)
-
-    def kernel_graphs(launch):
-        gs = []
-        with torch.cuda.stream(stream):
-            for s in range(sets):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    launch(s)
-                gs.append(g)
-        return gs
-
-    def time_graphs(gs):
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                gs[i % sets].replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for i in range(ks):
-                gs[i % sets].replay()
-            e1.record(stream)
-            e1.synchronize()
-        return e0.elapsed_time(e1) / ks
-
-    def launch_route(s):
-        q, k, v, out, idx = bufs[s]
-        bra.route(q, k, wl.S, wl.topk, idx=idx, stream=stream)
-
-    def launch_attend(s):
-        q, k, v, out, idx = bufs[s]
-        bra.attend(q, k, v, idx, wl.heads, wl.S, w, b, out=out, stream=stream)
-
-    route_ms = time_graphs(kernel_graphs(launch_route))
-    attend_ms = time_graphs(kernel_graphs(launch_attend))
+    route_ms = st.time_kernel(st.route, ks)
+    attend_ms = st.time_kernel(st.attend, ks)
 
     # end to end through the public API with pinned host buffers: copies in,
     # forward and copies out of consecutive batches overlapped (HostPipeline)
-    pipe = bra.HostPipeline(host[0].shape, tdt, wl.S, wl.topk, dev)
-    outs_h = [torch.empty(host[0].shape, dtype=tdt).pin_memory() for _ in range(2)]
+    host = st.host
+    pipe = bra.HostPipeline(host[0].shape, st.tdt, wl.S, wl.topk, dev)
+    outs_h = [torch.empty(host[0].shape, dtype=st.tdt).pin_memory() for _ in range(2)]
     es = max(1, args.e2e_steps)
     for i in range(3):
-        pipe.submit(*host, wl.heads, wl.S, wl.topk, w, b, outs_h[i % 2])
+        pipe.submit(*host, wl.heads, wl.S, wl.topk, st.w, st.b, outs_h[i % 2])
     pipe.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(pipe.copy_in)
     for i in range(es):
-        pipe.submit(*host, wl.heads, wl.S, wl.topk, w, b, outs_h[i % 2])
+        pipe.submit(*host, wl.heads, wl.S, wl.topk, st.w, st.b, outs_h[i % 2])
     e1.record(pipe.copy_out)
     e1.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -393,46 +579,63 @@ def our_arm(args, wl):
         e2e_ms = float(t.item())
     e2e_value = world * es * wl.tokens / (e2e_ms / 1e3)
     ok = bra.device_status(stream)
+    sets, set_bytes = st.sets, st.set_bytes
+    del pipe, outs_h
+    st.release()
 
     if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
-    peak, peak_kind = measured_peaks()
+    work = algorithmic_work(wl)
     dom = "attend" if attend_ms >= route_ms else "route"
     dom_ms = attend_ms if dom == "attend" else route_ms
-    achieved = ab[dom] / (dom_ms / 1e3) / 1e9
+    rl = roofline(work[dom], pk, wl.dtype, dom_ms * 1e-3)
     step_ms = ms / args.steps
+    elem = 2 if wl.dtype == "bf16" else 4
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-        if wl.dtype == "bf16" else "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic (seeded SplitMix64/Box-Muller: per-region N(0,1) offsets + "
                 "per-token N(0,0.5^2); LePE weights N(0,0.02^2))",
-        "config": {"workload": wl.name, **wl.describe(), "global_batch": wl.B * world,
+        "config": {"workload": wl.name, "config_number": CONFIG_NUMBER.get(wl.name),
+                   **wl.describe(), "global_batch": wl.B * world,
                    "l2": f"{sets} rotating input sets, {sets * set_bytes / 2**20:.0f} MiB "
                          f"> {L2_BYTES // 2**20} MiB L2",
-                   "launch": "cuda_graph" if graphs else "eager",
+                   "launch": "eager" if args.no_graph else "cuda_graph",
                    "parallelism": f"batch shards x{world}, no collective"},
-        "roofline": {"bound": "hbm", "kernel": f"bra_{dom}", "achieved": achieved,
-                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic(dom, wl.name),
-                     "algorithmic_bytes": ab[dom], "kernel_ms": dom_ms,
-                     "peak_source": f"hbm_gbs of MEASURED_PEAKS ({peak_kind})"},
-        "step_roofline": {"bytes": ab["forward"], "achieved_gbs": ab["forward"] / (step_ms / 1e3)
-                          / 1e9, "frac": ab["forward"] / (step_ms / 1e3) / 1e9 / peak},
+        "roofline": {**{k: rl[k] for k in ("bound", "achieved", "peak", "unit", "frac")},
+                     "traffic": recorded_traffic(dom, wl.name), "kernel": f"bra_{dom}",
+                     "algorithmic_bytes": work[dom]["bytes"], "kernel_ms": dom_ms,
+                     "terms_us": rl["terms_us"],
+                     "peak_source": f"MEASURED_PEAKS.json ({pk['source']}) for HBM and "
+                                    "tensor; ALU and MUFU from unit counts x max clock"},
+        "step_roofline": roofline(work["forward"], pk, wl.dtype, step_ms * 1e-3),
         "kernel_ms": {"bra_route": route_ms, "bra_attend": attend_ms},
         "e2e": {"value": e2e_value, "unit": "tokens/s",
-                "h2d_bytes_per_step": 3 * wl.tokens * wl.C * (2 if wl.dtype == "bf16" else 4),
-                "d2h_bytes_per_step": wl.tokens * wl.C * (2 if wl.dtype == "bf16" else 4),
+                "h2d_bytes_per_step": 3 * wl.tokens * wl.C * elem,
+                "d2h_bytes_per_step": wl.tokens * wl.C * elem,
                 "ms_per_step": e2e_ms / es},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "device_status": ok,
+        "peaks": pk,
     }
+    if world == 1:
+        line["launch_floor"] = launch_floor(torch, stream)
+        table = {}
+        for name in selected_workloads(args.workloads):
+            table[name] = measure_workload(bra_synth.WORKLOADS[name], dev, stream, pk,
+                                           ks, args.cpu_seconds_each, args.no_cpu,
+                                           not args.no_graph)
+        if table:
+            line["workloads"] = table
     if not args.no_cpu and world == 1:
         cores = os.cpu_count() or 1
-        xs = bra_synth.Inputs(x.q, x.k, x.v, x.lepe_w, x.lepe_b)
-        v_cpu, imgs, calls = time_oracle(wl, xs, args.cpu_seconds, cores)
+        v_cpu, imgs, calls = time_oracle(wl, x, args.cpu_seconds, cores)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "tokens/s", "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"first {imgs} image(s) of {wl.name}, {calls} "

@@ -36,8 +36,10 @@
  *              gave up, a routing index out of range) set a status word read
  *              by bra_device_status(). Nothing throws across the ABI.
  *   Aliasing   out must not overlap q, k or v.
- *   Threads    The library keeps no per-call state; calls on different
- *              streams may run concurrently.
+ *   Threads    Except for bra_forward_static, the library keeps no per-call
+ *              state: calls on different streams may run concurrently.
+ *              bra_forward_static keeps its routing index in one fixed
+ *              array per device, so its calls must not overlap on the GPU.
  *   Empty      B == 0 is valid and enqueues nothing.
  */
 #ifndef BRA_H_
@@ -157,6 +159,20 @@ const char *bra_status_string(int status);
 
 /* Version of this ABI (major * 100 + minor). */
 int bra_abi_version(void);
+
+/*
+ * bra_check_wait_timeout -- exercises the device-side failure path without a
+ * fault: enqueues one small kernel whose bounded mbarrier wait can never
+ * complete (it expects bytes that no copy delivers). The wait gives up after
+ * limit_ns nanoseconds of the GPU's global timer, sets the timeout bit of the
+ * device status word and the kernel returns; bra_device_status then reports
+ * BRA_ERR_TIMEOUT (clear the word before further work: after a timeout,
+ * later waits that do not succeed at once return without waiting).
+ *   limit_ns  1000 .. 1e9, otherwise BRA_ERR_INVALID_ARG and nothing is
+ *             enqueued.
+ * No page describes it; it tests this library's own error reporting.
+ */
+int bra_check_wait_timeout(uint64_t limit_ns, void *stream);
 
 #ifdef __cplusplus
 }

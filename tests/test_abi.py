@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.bra_abi_version() == 100
+    assert lib.bra_abi_version() == 101
     assert bra.status_string(0) == "ok"
     assert "unsupported" in bra.status_string(2)
     assert bra.status_string(99) == "unknown status"
@@ -114,3 +114,9 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(bra, "_lib", None)
     with pytest.raises(ImportError):
         bra._load()
+
+
+def test_wait_timeout_check_rejects_bad_limits(lib):
+    assert lib.bra_check_wait_timeout(0, NULL) == bra.BRA_ERR_INVALID_ARG
+    assert lib.bra_check_wait_timeout(999, NULL) == bra.BRA_ERR_INVALID_ARG
+    assert lib.bra_check_wait_timeout(1_000_000_001, NULL) == bra.BRA_ERR_INVALID_ARG

@@ -75,3 +75,69 @@ def test_clock_summary_short_window_and_no_samples():
     s.rows = [(0.1, _row(2032)), (0.2, _row(2030)), (5.0, _row(2032))]
     out = s.summary(4.9, 5.1, "timed region")
     assert out["samples"] == 3 and "too short" in out["window"]
+
+
+# Per-forward algorithmic work of the five workloads, as tabled for the
+# roofline: bytes, contraction GFLOP, other float32 GFLOP and exponentials.
+SURVEY_TABLE = {
+    "tiny_f32": (0.21e6, 0.0008, 0.0010, 6.3e3),
+    "stage1_bf16": (102.8e6, 3.29, 0.68, 25.7e6),
+    "stage2_bf16": (51.4e6, 1.64, 0.38, 12.8e6),
+    "stage3_bf16": (25.7e6, 0.82, 0.25, 6.4e6),
+    "seg512_bf16": (67.1e6, 8.59, 0.50, 67.1e6),
+}
+
+
+def test_algorithmic_work_matches_the_tabled_counts():
+    for name, (nbytes, tc, alu, exps) in SURVEY_TABLE.items():
+        wl = bra_synth.WORKLOADS[name]
+        w = bench.algorithmic_work(wl)["forward"]
+        assert abs(w["bytes"] - nbytes) / nbytes < 0.05, name  # tabled to 2-4 digits
+        assert abs(w["exps"] - exps) / exps < 0.01, name
+        if wl.dtype == "bf16":
+            assert abs(w["tensor_flops"] / 1e9 - tc) / tc < 0.01, name
+            assert abs(w["alu_flops"] / 1e9 - alu) / alu < 0.02, name
+        else:  # the float32 path contracts on the FMA pipe
+            assert w["tensor_flops"] == 0
+            assert abs(w["alu_flops"] / 1e9 - (tc + alu)) / (tc + alu) < 0.05, name
+    # the kernels' shares add up to the forward
+    w = bench.algorithmic_work(bra_synth.WORKLOADS["stage3_bf16"])
+    assert w["route"]["alu_flops"] + w["attend"]["alu_flops"] == w["forward"]["alu_flops"]
+    assert w["attend"]["exps"] == w["forward"]["exps"]
+
+
+def test_roofline_takes_the_slowest_pipe():
+    pk = {"hbm_gbs": 6500.0, "tensor_tflops": 1750.0, "alu_tflops": 77.0,
+          "ex2_per_s_f32": 4.8e12, "ex2_per_s_bf16": 9.6e12}
+    hbm_bound = {"bytes": 65e6, "tensor_flops": 1e9, "alu_flops": 1e8, "exps": 1e6}
+    r = bench.roofline(hbm_bound, pk, "bf16", 20e-6)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["roof_us"] - 10.0) < 1e-9 and abs(r["frac"] - 0.5) < 1e-9
+    assert abs(r["achieved"] - 3250.0) < 1e-6 and r["peak"] == 6500.0
+    alu_bound = {"bytes": 6.5e6, "tensor_flops": 0, "alu_flops": 7.7e8, "exps": 0}
+    r = bench.roofline(alu_bound, pk, "f32", 40e-6)
+    assert r["bound"] == "alu" and abs(r["roof_us"] - 10.0) < 1e-9
+    assert abs(r["frac"] - 0.25) < 1e-9
+    mufu_bound = {"bytes": 0, "tensor_flops": 0, "alu_flops": 0, "exps": 9.6e7}
+    assert bench.roofline(mufu_bound, pk, "bf16", 1e-5)["bound"] == "mufu"
+    assert abs(bench.roofline(mufu_bound, pk, "f32", 1e-5)["roof_us"] - 20.0) < 1e-9
+
+
+def test_peaks_derive_alu_and_mufu_from_unit_counts(tmp_path, monkeypatch):
+    p = tmp_path / "peaks.json"
+    p.write_text(json.dumps({"hbm_gbs": 6492.7, "bf16_tflops": 1744.1, "sm_max_mhz": 2032.0}))
+    monkeypatch.setattr(bench, "PEAKS_FILE", str(p))
+    pk = bench.peaks(148)
+    assert pk["source"] == "measured" and pk["hbm_gbs"] == 6492.7
+    assert abs(pk["alu_tflops"] - 148 * 128 * 2 * 2.032e9 / 1e12) < 1e-9
+    assert abs(pk["ex2_per_s_bf16"] - 2 * pk["ex2_per_s_f32"]) < 1.0
+    assert abs(pk["ex2_per_s_f32"] - 148 * 16 * 2.032e9) < 1.0
+
+
+def test_workload_selection_and_config_numbers():
+    assert bench.selected_workloads("all") == list(bra_synth.WORKLOADS)
+    assert bench.selected_workloads("none") == []
+    assert bench.selected_workloads("tiny_f32, stage3_bf16") == ["tiny_f32", "stage3_bf16"]
+    assert bench.CONFIG_NUMBER["tiny_f32"] == 1 and bench.CONFIG_NUMBER["stage3_bf16"] == 4
+    args = bench.parse_args([])
+    assert args.workload == "stage1_bf16" and args.workloads == "all"

@@ -8,6 +8,9 @@ than 16 tokens and whose 64-channel chunk fits in shared memory take the
 image-resident attend kernel (the image_* and n4 / ragged_n15 shapes); the
 others take the region kernel.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -56,6 +59,11 @@ def test_full_workloads_match_oracle(name, cuda_device):
     wl = bra_synth.WORKLOADS[name]
     res = run_and_compare(wl, cuda_device, seed=0)
     print(name, res)
+    record = os.environ.get("BRA_PARITY_RECORD")
+    if record:  # a JSON line per workload: the measured errors against the oracle
+        with open(record, "a") as f:
+            f.write(json.dumps({"workload": name, "seed": 0, "tolerance": TOL[wl.dtype],
+                                **res}) + "\n")
     # with these value distributions near-ties are rare
     assert res["rows_near_tie"] <= max(2, res["rows"] // 1000)
 

@@ -16,7 +16,8 @@ import torch
 
 __all__ = ["BraError", "route", "attend", "forward", "forward_static", "forward_host",
            "HostPipeline",
-           "idx_workspace_bytes", "device_status", "library_path", "SYMBOLS"]
+           "idx_workspace_bytes", "device_status", "check_wait_timeout", "library_path",
+           "SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libbra.so")
@@ -35,6 +36,7 @@ SYMBOLS = {
     "bra_device_status": (_I, [_P, _I]),
     "bra_status_string": (ctypes.c_char_p, [_I]),
     "bra_abi_version": (_I, []),
+    "bra_check_wait_timeout": (_I, [ctypes.c_uint64, _P]),
 }
 
 _lib = None
@@ -240,6 +242,12 @@ class HostPipeline:
 
     def synchronize(self):
         self.copy_out.synchronize()
+
+
+def check_wait_timeout(limit_ns: int = 2_000_000, stream=None) -> None:
+    """Enqueues a kernel whose bounded wait must give up after limit_ns; the
+    next device_status() reports BRA_ERR_TIMEOUT (see include/bra.h)."""
+    _check(_load().bra_check_wait_timeout(limit_ns, _stream(stream)), "bra_check_wait_timeout")
 
 
 def device_status(stream=None, clear: bool = True) -> int:

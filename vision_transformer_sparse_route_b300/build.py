@@ -13,7 +13,7 @@ LIB = os.path.join(PKG, "libbra.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 SOURCES = ["bra.cu"]
-DEPS = ["bra.cu", "ptx.cuh", "route.cuh", "attend_bf16.cuh", "attend_f32.cuh",
+DEPS = ["bra.cu", "ptx.cuh", "route.cuh", "attend_bf16.cuh", "attend_f32.cuh", "per_device.h",
         "attend_image.cuh"]
 
 

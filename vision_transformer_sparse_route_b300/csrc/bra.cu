@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "bra.h"
+#include "per_device.h"
 #include "attend_bf16.cuh"
 #include "attend_f32.cuh"
 #include "attend_image.cuh"
@@ -102,16 +103,17 @@ bool make_map(CUtensorMap *m, const void *base, int B, int H, int W, int C,
 }
 
 // Raises a kernel's dynamic shared-memory limit to the per-block maximum,
-// once per kernel and process.
+// once per kernel and device (the attribute holds per device context).
 cudaError_t allow_smem(const void *kernel, size_t bytes) {
-  static std::mutex mu;
-  static std::vector<const void *> done;
+  static bra::PerDeviceOnce once;
   if (bytes <= 48 * 1024) return cudaSuccess;
-  std::lock_guard<std::mutex> lock(mu);
-  if (std::find(done.begin(), done.end(), kernel) != done.end()) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(
-      kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmemPerBlock);
-  if (e == cudaSuccess) done.push_back(kernel);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (once.done(dev, kernel)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kMaxSmemPerBlock);
+  if (e == cudaSuccess) once.mark(dev, kernel);
   return e;
 }
 
@@ -235,16 +237,16 @@ int launch_route_dtype(const void *q, const void *k, int B, int CL, const bra::R
   return launch_route_t<T, 32>(q, k, B, CL, g, smem, local_k, idx, aff, s);
 }
 
-// Lets a kernel use clusters of 16 CTAs (once per kernel and process).
+// Lets a kernel use clusters of 16 CTAs (once per kernel and device).
 bool allow_wide_clusters(const void *kernel) {
-  static std::mutex mu;
-  static std::vector<const void *> done;
-  std::lock_guard<std::mutex> lock(mu);
-  if (std::find(done.begin(), done.end(), kernel) != done.end()) return true;
+  static bra::PerDeviceOnce once;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (once.done(dev, kernel)) return true;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
       cudaSuccess)
     return false;
-  done.push_back(kernel);
+  once.mark(dev, kernel);
   return true;
 }
 
@@ -726,7 +728,14 @@ const char *bra_status_string(int status) {
   }
 }
 
-int bra_abi_version(void) { return 100; }
+int bra_abi_version(void) { return 101; }
+
+int bra_check_wait_timeout(uint64_t limit_ns, void *stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000ull) return BRA_ERR_INVALID_ARG;
+  (void)cudaGetLastError();
+  bra::bra_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns);
+  return cuda_status(cudaGetLastError());
+}
 
 }  // extern "C"
 

@@ -64,19 +64,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
+// Waits for phase `parity` of `bar` to complete, for at most limit_ns.
 // On giving up it sets kStatusTimeout and returns false; the caller carries
 // on (so that every thread still reaches every barrier of the block). Once
 // the timeout bit is set (until the host clears it), waits that do not
 // succeed at once return false immediately, so a launch that went wrong ends
 // quickly instead of timing out wait by wait.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   // after one wait of this launch has given up, later ones do not wait again
   if (*reinterpret_cast<volatile unsigned *>(&g_status) & kStatusTimeout) return false;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(&g_status, kStatusTimeout);
       return false;
     }
@@ -183,6 +184,25 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) {
 // chunk index is XORed with the row index modulo 8.
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+}  // namespace bra
+
+namespace bra {
+
+// One warp; its first thread waits on an mbarrier phase that expects 16
+// bytes of copies none of which is ever issued, so the bounded wait gives up
+// after limit_ns, sets kStatusTimeout and the kernel returns normally. It
+// exercises the device-side failure path without a fault.
+__global__ void bra_wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, 16);
+    mbar_wait(&bar, 0, limit_ns);
+  }
+  __syncwarp();
 }
 
 }  // namespace bra
