@@ -356,6 +356,11 @@ class Setup:
         self.bra.forward(q, k, v, self.wl.heads, self.wl.S, self.wl.topk, self.w, self.b,
                          out=out, idx=idx, stream=self.stream)
 
+    def launches(self) -> int:
+        wl = self.wl
+        return self.bra.forward_launches(wl.B, wl.H, wl.W, wl.C, wl.heads, wl.S, wl.topk,
+                                         wl.ks, 1 if wl.dtype == "bf16" else 0)
+
     def route(self, s):
         q, k, v, out, idx = self.bufs[s % self.sets]
         self.bra.route(q, k, self.wl.S, self.wl.topk, idx=idx, stream=self.stream)
@@ -462,12 +467,15 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
     ms = st.time_steps(n) / n
     route_ms = st.time_kernel(st.route, kernel_steps)
     attend_ms = st.time_kernel(st.attend, kernel_steps)
+    fwd_ms = st.time_kernel(st.fwd, kernel_steps)
     work = algorithmic_work(wl)
     ok = st.bra.device_status(stream)
+    launches = st.launches()
     st.release()
     del st
     entry = {"config": CONFIG_NUMBER.get(wl.name), "ms_per_step": ms, "steps_timed": n,
-             "tokens_per_s": wl.tokens / (ms * 1e-3), "route_us": route_ms * 1e3,
+             "tokens_per_s": wl.tokens / (ms * 1e-3), "forward_launches": launches,
+             "forward_us": fwd_ms * 1e3, "route_us": route_ms * 1e3,
              "attend_us": attend_ms * 1e3,
              "step_roofline": roofline(work["forward"], pk, wl.dtype, ms * 1e-3),
              "route_roofline": roofline(work["route"], pk, wl.dtype, route_ms * 1e-3),
@@ -554,6 +562,8 @@ def our_arm(args, wl):
     ks = max(1, args.kernel_steps)
     route_ms = st.time_kernel(st.route, ks)
     attend_ms = st.time_kernel(st.attend, ks)
+    launches = st.launches()
+    fwd_ms = st.time_kernel(st.fwd, ks) if launches == 1 else None
 
     # end to end through the public API with pinned host buffers: copies in,
     # forward and copies out of consecutive batches overlapped (HostPipeline)
@@ -589,8 +599,11 @@ def our_arm(args, wl):
             dist.destroy_process_group()
         return
     work = algorithmic_work(wl)
-    dom = "attend" if attend_ms >= route_ms else "route"
-    dom_ms = attend_ms if dom == "attend" else route_ms
+    if launches == 1:  # the forward is one kernel (routing inside it)
+        dom, dom_ms = "forward", fwd_ms
+    else:
+        dom = "attend" if attend_ms >= route_ms else "route"
+        dom_ms = attend_ms if dom == "attend" else route_ms
     rl = roofline(work[dom], pk, wl.dtype, dom_ms * 1e-3)
     step_ms = ms / args.steps
     elem = 2 if wl.dtype == "bf16" else 4
@@ -614,12 +627,14 @@ def our_arm(args, wl):
                      "peak_source": f"MEASURED_PEAKS.json ({pk['source']}) for HBM and "
                                     "tensor; ALU and MUFU from unit counts x max clock"},
         "step_roofline": roofline(work["forward"], pk, wl.dtype, step_ms * 1e-3),
-        "kernel_ms": {"bra_route": route_ms, "bra_attend": attend_ms},
+        "kernel_ms": {"bra_route": route_ms, "bra_attend": attend_ms,
+                      **({"bra_forward": fwd_ms} if fwd_ms is not None else {})},
+        "forward_launches": launches,
         "e2e": {"value": e2e_value, "unit": "tokens/s",
                 "h2d_bytes_per_step": 3 * wl.tokens * wl.C * elem,
                 "d2h_bytes_per_step": wl.tokens * wl.C * elem,
                 "ms_per_step": e2e_ms / es},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "device_status": ok,
         "peaks": pk,

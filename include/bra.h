@@ -103,10 +103,16 @@ int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
                void *out, void *stream);
 
 /*
- * bra_forward -- bra_route then bra_attend on one stream.
+ * bra_forward -- the whole forward: the routing of bra_route, then the
+ * attention of bra_attend, on one stream.
  *   idx_workspace  device buffer of bra_idx_workspace_bytes(B, S, topk)
- *                  bytes; receives the routing index.
- * Other arguments as above.
+ *                  bytes; receives the routing index, the same bit for bit
+ *                  as bra_route's.
+ * Other arguments as above. bf16 maps that the image-resident attend kernel
+ * takes, with at most 64 regions, C in {64, 128, 256} and few enough images
+ * that one cluster of C / 64 CTAs per image is resident at once on the device,
+ * run as one kernel with the routing computed inside it; other problems run
+ * the routing kernel and then the attend kernel.
  */
 int bra_forward(const void *q, const void *k, const void *v, int B, int H,
                 int W, int C, int heads, int S, int topk, const float *lepe_w,
@@ -141,6 +147,15 @@ int bra_forward_static(const void *q, const void *k, const void *v, int B,
                        int H, int W, int C, int heads, int S, int topk,
                        const float *lepe_w, const float *lepe_b, int lepe_ks,
                        int dtype, void *out, void *stream);
+
+/*
+ * bra_forward_launches -- how many kernels bra_forward (and
+ * bra_forward_static) enqueue for this problem on the current device: 1 or 2,
+ * 0 for B == 0, or minus a status code for invalid sizes. Nothing is
+ * enqueued (it may query the device's occupancy once).
+ */
+int bra_forward_launches(int B, int H, int W, int C, int heads, int S, int topk, int lepe_ks,
+                         int dtype);
 
 /* Bytes of the routing index [B, S*S, topk] int32; 0 on invalid sizes. */
 size_t bra_idx_workspace_bytes(int B, int S, int topk);

@@ -16,7 +16,7 @@ import torch
 
 __all__ = ["BraError", "route", "attend", "forward", "forward_static", "forward_host",
            "HostPipeline",
-           "idx_workspace_bytes", "device_status", "check_wait_timeout", "library_path",
+           "idx_workspace_bytes", "forward_launches", "device_status", "check_wait_timeout", "library_path",
            "SYMBOLS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +33,7 @@ SYMBOLS = {
     "bra_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
     "bra_forward_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "bra_idx_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "bra_forward_launches": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "bra_device_status": (_I, [_P, _I]),
     "bra_status_string": (ctypes.c_char_p, [_I]),
     "bra_abi_version": (_I, []),
@@ -105,6 +106,15 @@ def _map(t: torch.Tensor, name: str):
 
 def idx_workspace_bytes(B: int, S: int, topk: int) -> int:
     return _load().bra_idx_workspace_bytes(B, S, topk)
+
+
+def forward_launches(B: int, H: int, W: int, C: int, heads: int, S: int, topk: int,
+                     lepe_ks: int, dtype: int = BRA_BF16) -> int:
+    """Kernels one bra_forward enqueues for this problem (1 or 2)."""
+    n = _load().bra_forward_launches(B, H, W, C, heads, S, topk, lepe_ks, dtype)
+    if n < 0:
+        raise BraError(-n, "bra_forward_launches")
+    return n
 
 
 def route(q, k, S: int, topk: int, idx=None, affinity=None, stream=None):

@@ -17,12 +17,14 @@
 #include "attend_bf16.cuh"
 #include "attend_f32.cuh"
 #include "attend_image.cuh"
+#include "forward_image.cuh"
 #include "route.cuh"
 
 namespace {
 
 using bra::AttendF32Geom;
 using bra::AttendGeom;
+using bra::FusedGeom;
 using bra::ImageGeom;
 
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;
@@ -457,6 +459,41 @@ bool plan_attend_image(int H, int W, int C, int heads, int S, int topk, int ks,
   return *smem <= kMaxSmemPerBlock;
 }
 
+// The one-launch forward (routing inside the image-resident attend kernel):
+// bf16 maps the image kernel takes, at most 64 regions, and channel counts the
+// routing kernel supports (C / 64 CTAs in a cluster per image: 1, 2 or 4).
+bool plan_forward_image(int H, int W, int C, int heads, int S, int topk, int ks,
+                        FusedGeom *fg, size_t *smem) {
+  ImageGeom a;
+  size_t s0;
+  if (!plan_attend_image(H, W, C, heads, S, topk, ks, &a, &s0)) return false;
+  const int G = route_groups(C, BRA_BF16);
+  if (!G || a.R > 64 || (a.nc != 1 && a.nc != 2 && a.nc != 4)) return false;
+  FusedGeom f = {};
+  f.L = 32 / G;
+  f.inv_n = 1.0f / static_cast<float>(a.n);
+  const size_t tokens = (size_t)H * W;
+  f.rp = (a.R + 3) / 4 * 4;
+  // the routing scratch (means, this CTA's rows of the affinity) shares the
+  // area of the f32 O tile, which is written only after the routing
+  const size_t rows = (size_t)(a.R + a.nc - 1) / a.nc;
+  const size_t routing = (size_t)2 * 64 * f.rp * 4 + rows * a.R * 4;
+  f.off_qm = a.off_o;
+  f.off_km = f.off_qm + 64 * f.rp * 4;
+  f.off_a = f.off_km + 64 * f.rp * 4;
+  a.off_w = (uint32_t)round_up((size_t)a.off_o + std::max(tokens * 64 * 4, routing), 16);
+  a.off_tab = (uint32_t)round_up((size_t)a.off_w + (size_t)(ks * ks + 1) * 64 * 4, 16);
+  f.off_p = (uint32_t)round_up((size_t)a.off_tab + (size_t)a.R * a.nkp * 2, 16);
+  f.off_ridx = (uint32_t)round_up((size_t)f.off_p + (size_t)a.R * a.R * 4, 16);
+  f.off_tok = (uint32_t)round_up((size_t)f.off_ridx + (size_t)a.R * topk * 4, 16);
+  f.off_bar = (uint32_t)round_up((size_t)f.off_tok + (64 + 16) * 2, 8);
+  a.off_bar = f.off_bar;
+  f.img = a;
+  *smem = (size_t)f.off_bar + 16 + 1024;  // slack to align the base to 1024 bytes
+  *fg = f;
+  return *smem <= kMaxSmemPerBlock;
+}
+
 bool plan_attend_f32(int H, int W, int C, int heads, int S, int topk, int ks,
                      AttendF32Geom *g, size_t *smem) {
   if (C % 4 || C / heads > 64) return false;
@@ -566,6 +603,125 @@ int launch_attend_image_ks(const void *q, const void *k, const void *v,
   if (g.H % 7 == 0)
     return launch_attend_image_kr<KS, 7>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
   return launch_attend_image_kr<KS, 8>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
+}
+
+template <int KS, int RB>
+int launch_forward_image_kr(const void *q, const void *k, const void *v, int32_t *idx, int B,
+                            const float *w, const float *bias, void *out, const FusedGeom &f,
+                            size_t smem, cudaStream_t s) {
+  const ImageGeom &g = f.img;
+  CUtensorMap tq, tk, tv, th;
+  if (!make_map(&tq, q, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map(&tk, k, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map(&tv, v, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map(&th, v, B, g.H, g.W, g.C, g.halo_w, g.halo_h, false))
+    return BRA_ERR_CUDA;
+  auto kern = bra::bra_forward_image_kernel<KS, RB>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((size_t)B * g.nc), 1, 1);
+  cfg.blockDim = dim3(bra::kImgThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = g.nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, th,
+                                        static_cast<__nv_bfloat16 *>(out), idx, w, bias, f));
+}
+
+template <int KS>
+int launch_forward_image_ks(const void *q, const void *k, const void *v, int32_t *idx, int B,
+                            const float *w, const float *bias, void *out, const FusedGeom &f,
+                            size_t smem, cudaStream_t s) {
+  if (f.img.H % 7 == 0)
+    return launch_forward_image_kr<KS, 7>(q, k, v, idx, B, w, bias, out, f, smem, s);
+  return launch_forward_image_kr<KS, 8>(q, k, v, idx, B, w, bias, out, f, smem, s);
+}
+
+int launch_attend(const void *q, const void *k, const void *v, const int32_t *idx,
+                  int B, int H, int W, int C, int heads, int S, int topk,
+                  const float *w, const float *bias, int ks, int dtype, void *out,
+                  bool pdl, cudaStream_t s);
+
+// Whether all B clusters of the one-launch forward are resident at once on
+// the current device (asked once per device and cluster shape). With more
+// images the clusters run in waves, each as long as a whole cluster's
+// routing, attention and LePE, and the routing kernel plus the attend kernel
+// (whose CTAs need no partners) finish sooner.
+bool forward_image_one_wave(int B, const FusedGeom &f, size_t smem) {
+  struct Entry { int dev, nc; size_t smem; int clusters; };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const int nc = f.img.nc;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &e : cache)
+      if (e.dev == dev && e.nc == nc && e.smem == smem) return B <= e.clusters;
+  }
+  // every instantiation has the same block shape and shared memory
+  const void *kern = reinterpret_cast<const void *>(bra::bra_forward_image_kernel<5, 7>);
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nc, 1, 1);
+  cfg.blockDim = dim3(bra::kImgThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (allow_smem(kern, smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+    n = 0;
+  (void)cudaGetLastError();
+  std::lock_guard<std::mutex> lock(mu);
+  cache.push_back({dev, nc, smem, n});
+  return B <= n;
+}
+
+// The forward's launches: one kernel where the shape allows it, else the
+// routing kernel and then the attend kernel (programmatic dependent launch).
+int launch_forward(const void *q, const void *k, const void *v, int B, int H, int W, int C,
+                   int heads, int S, int topk, const float *w, const float *bias, int ks,
+                   int dtype, int32_t *idx, void *out, cudaStream_t s) {
+  FusedGeom f;
+  size_t smem;
+  if (dtype == BRA_BF16 && plan_forward_image(H, W, C, heads, S, topk, ks, &f, &smem) &&
+      forward_image_one_wave(B, f, smem)) {
+    switch (ks) {
+      case 1: return launch_forward_image_ks<1>(q, k, v, idx, B, w, bias, out, f, smem, s);
+      case 3: return launch_forward_image_ks<3>(q, k, v, idx, B, w, bias, out, f, smem, s);
+      case 5: return launch_forward_image_ks<5>(q, k, v, idx, B, w, bias, out, f, smem, s);
+      default: return launch_forward_image_ks<7>(q, k, v, idx, B, w, bias, out, f, smem, s);
+    }
+  }
+  int rc = launch_route(q, k, B, H, W, C, S, topk, dtype, idx, nullptr, s);
+  if (rc) return rc;
+  // programmatic dependent launch: the attend grid may start while the route
+  // grid drains; it waits for that grid only where it reads the routing index
+  return launch_attend(q, k, v, idx, B, H, W, C, heads, S, topk, w, bias, ks, dtype, out,
+                       true, s);
+}
+
+// Kernels bra_forward launches for a shape (1 or 2).
+int forward_launches(int B, int H, int W, int C, int heads, int S, int topk, int ks,
+                     int dtype) {
+  FusedGeom f;
+  size_t smem;
+  return (dtype == BRA_BF16 && plan_forward_image(H, W, C, heads, S, topk, ks, &f, &smem) &&
+          forward_image_one_wave(B, f, smem))
+             ? 1
+             : 2;
 }
 
 template <int KS>
@@ -687,13 +843,17 @@ int bra_forward(const void *q, const void *k, const void *v, int B, int H, int W
       overlap(idx_workspace, ib, k, bytes) || overlap(idx_workspace, ib, v, bytes))
     return BRA_ERR_INVALID_ARG;
   (void)cudaGetLastError();
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = launch_route(q, k, B, H, W, C, S, topk, dtype, idx_workspace, nullptr, s);
-  if (rc) return rc;
-  // programmatic dependent launch: the attend grid may start while the route
-  // grid drains; it waits for that grid only where it reads the routing index
-  return launch_attend(q, k, v, idx_workspace, B, H, W, C, heads, S, topk, lepe_w,
-                       lepe_b, lepe_ks, dtype, out, true, s);
+  return launch_forward(q, k, v, B, H, W, C, heads, S, topk, lepe_w, lepe_b, lepe_ks, dtype,
+                        idx_workspace, out, static_cast<cudaStream_t>(stream));
+}
+
+int bra_forward_launches(int B, int H, int W, int C, int heads, int S, int topk, int lepe_ks,
+                         int dtype) {
+  int rc = check_map_args(B, H, W, C, S, topk, dtype);
+  if (rc) return -rc;
+  if (heads <= 0 || C % heads || lepe_ks <= 0 || lepe_ks % 2 == 0) return -BRA_ERR_INVALID_ARG;
+  if (B == 0) return 0;
+  return forward_launches(B, H, W, C, heads, S, topk, lepe_ks, dtype);
 }
 
 size_t bra_idx_workspace_bytes(int B, int S, int topk) {
@@ -786,9 +946,6 @@ extern "C" int bra_forward_static(const void *q, const void *k, const void *v, i
   int32_t *idx = static_idx_address();
   if (!idx) return BRA_ERR_CUDA;
   (void)cudaGetLastError();
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = launch_route(q, k, B, H, W, C, S, topk, dtype, idx, nullptr, s);
-  if (rc) return rc;
-  return launch_attend(q, k, v, idx, B, H, W, C, heads, S, topk, lepe_w, lepe_b,
-                       lepe_ks, dtype, out, true, s);
+  return launch_forward(q, k, v, B, H, W, C, heads, S, topk, lepe_w, lepe_b, lepe_ks, dtype,
+                        idx, out, static_cast<cudaStream_t>(stream));
 }

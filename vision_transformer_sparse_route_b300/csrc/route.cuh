@@ -16,7 +16,11 @@
 // shared memory; for grids too large to copy, it reads them from the peers in
 // place), and computes the affinity rows and the top-k of its own regions.
 // Nothing goes through global memory but the inputs and the outputs.
-// Arithmetic is float32 with FMA in a fixed order.
+// Arithmetic is float32 in a fixed order: a region mean sums its tokens in
+// L = 32 / G interleaved partial sums (lane j of a channel group takes the
+// tokens t = j, j + L, ... in row-major order), adds the partials pairwise
+// (j with j ^ 1, then with j ^ 2, ...) and multiplies by 1/n; the affinity
+// follows kAffChunk below.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -35,6 +39,12 @@ constexpr int kRouteThreadsFew = 512;
 constexpr int kRouteUnroll = 8;  // 16-byte loads a lane keeps in flight
 
 constexpr int kAffRows = 4;  // owned rows of one affinity tile
+
+// The affinity A[i][j] = sum_c Qm[i][c] Km[j][c] is formed as one float32 FMA
+// chain per run of kAffChunk channels (in channel order, from zero), and the
+// chains' results are added in run order. Every kernel that computes the
+// routing follows this order, so that their routing indices agree bit for bit.
+constexpr int kAffChunk = 64;
 
 struct RouteGeom {
   int H, W, C, S, topk;
@@ -123,6 +133,77 @@ __device__ __forceinline__ void pool_region(const uint4 *base, size_t row_stride
   }
 }
 
+// The top-k of one affinity row, chosen by one warp: columns in order of
+// decreasing value, equal values by increasing column; a NaN never wins.
+// val[t] holds the row's value at column lane + 32 t (-inf from column R on,
+// NaN already replaced by -inf). When the row also sits in shared memory
+// (row != nullptr), the grid is small (R <= 64) and many regions are routed
+// (topk > 4), each lane ranks its values against the whole row (one
+// broadcast load per column, no shuffles) and writes each to its place;
+// otherwise topk rounds of a warp arg-max. The topk columns go to dst (and
+// to dst2 when given).
+template <int MAXJ>
+__device__ __forceinline__ void select_topk(const float (&val)[MAXJ], const float *row, int R,
+                                            int topk, int lane, int32_t *dst, int32_t *dst2) {
+  if (row && R <= 64 && topk > 4) {
+    int rank_of[MAXJ];
+#pragma unroll
+    for (int t = 0; t < MAXJ; ++t) rank_of[t] = 0;
+    // eight columns at a time, their loads issued together
+    for (int jj0 = 0; jj0 < R; jj0 += 8) {
+      float a8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a8[u] = row[min(jj0 + u, R - 1)];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int jj = jj0 + u;
+        const float a = (a8[u] == a8[u]) ? a8[u] : -INFINITY;
+#pragma unroll
+        for (int t = 0; t < MAXJ; ++t) {
+          const int j = lane + 32 * t;
+          rank_of[t] += (jj < R && (a > val[t] || (a == val[t] && jj < j))) ? 1 : 0;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < MAXJ; ++t) {
+      const int j = lane + 32 * t;
+      if (j < R && rank_of[t] < topk) {
+        dst[rank_of[t]] = j;
+        if (dst2) dst2[rank_of[t]] = j;
+      }
+    }
+    return;
+  }
+  unsigned taken = 0;  // bit t: column lane + 32 t already chosen
+  for (int m = 0; m < topk; ++m) {
+    float bv = -INFINITY;
+    int bj = 0x7fffffff;
+#pragma unroll
+    for (int t = 0; t < MAXJ; ++t) {
+      const int j = lane + 32 * t;
+      if (j < R && !((taken >> t) & 1u) && (val[t] > bv || (val[t] == bv && j < bj))) {
+        bv = val[t];
+        bj = j;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
+      if (ov > bv || (ov == bv && oj < bj)) {
+        bv = ov;
+        bj = oj;
+      }
+    }
+    if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
+    if (lane == 0) {
+      dst[m] = bj;
+      if (dst2) dst2[m] = bj;
+    }
+  }
+}
+
 // Grid (CL, B), cluster (CL, 1, 1), NT threads.
 // MAXJ = ceil(R / 32): affinity values each lane keeps for the top-k.
 // LOCAL_K: copy every K mean into local shared memory first (fast path);
@@ -201,27 +282,33 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
       const int r0 = (t / ctiles) * kAffRows, j = (t % ctiles) * 32 + lane;
       const float *kj = kall + min(j, R - 1) * (C + 1);
       const float *q0 = qm + min(r0, ro - 1) * C;
-      float acc[kAffRows];
+      float tot[kAffRows];
+      for (int c0 = 0; c0 < C; c0 += kAffChunk) {
+        const int c1 = min(c0 + kAffChunk, C);
+        float acc[kAffRows];
 #pragma unroll
-      for (int r = 0; r < kAffRows; ++r) acc[r] = 0.f;
+        for (int r = 0; r < kAffRows; ++r) acc[r] = 0.f;
 #pragma unroll 2
-      for (int c = 0; c < C; c += 4) {
-        const float k0 = kj[c], k1 = kj[c + 1], k2 = kj[c + 2], k3 = kj[c + 3];
+        for (int c = c0; c < c1; c += 4) {
+          const float k0 = kj[c], k1 = kj[c + 1], k2 = kj[c + 2], k3 = kj[c + 3];
 #pragma unroll
-        for (int r = 0; r < kAffRows; ++r) {
-          // rows past the owned ones repeat the last (their results are dropped)
-          const float4 q4 = *reinterpret_cast<const float4 *>(
-              q0 + (r0 + r < ro ? r : 0) * C + c);
-          float a = fmaf(q4.x, k0, acc[r]);
-          a = fmaf(q4.y, k1, a);
-          a = fmaf(q4.z, k2, a);
-          acc[r] = fmaf(q4.w, k3, a);
+          for (int r = 0; r < kAffRows; ++r) {
+            // rows past the owned ones repeat the last (their results are dropped)
+            const float4 q4 = *reinterpret_cast<const float4 *>(
+                q0 + (r0 + r < ro ? r : 0) * C + c);
+            float a = fmaf(q4.x, k0, acc[r]);
+            a = fmaf(q4.y, k1, a);
+            a = fmaf(q4.z, k2, a);
+            acc[r] = fmaf(q4.w, k3, a);
+          }
         }
+#pragma unroll
+        for (int r = 0; r < kAffRows; ++r) tot[r] = c0 == 0 ? acc[r] : tot[r] + acc[r];
       }
       if (j < R)
 #pragma unroll
         for (int r = 0; r < kAffRows; ++r)
-          if (r0 + r < ro) arow[(r0 + r) * R + j] = acc[r];
+          if (r0 + r < ro) arow[(r0 + r) * R + j] = tot[r];
     }
     __syncthreads();
   }
@@ -241,12 +328,18 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
         kj[t] = LOCAL_K ? kall + j * (C + 1)
                         : cluster.map_shared_rank(km, j % CL) + (j / CL) * C;
       }
+      for (int c0 = 0; c0 < C; c0 += kAffChunk) {
+        const int c1 = min(c0 + kAffChunk, C);
+        float acc[MAXJ];
 #pragma unroll
-      for (int t = 0; t < MAXJ; ++t) dot[t] = 0.f;
-      for (int c = 0; c < C; ++c) {
-        const float qc = qi[c];
+        for (int t = 0; t < MAXJ; ++t) acc[t] = 0.f;
+        for (int c = c0; c < c1; ++c) {
+          const float qc = qi[c];
 #pragma unroll
-        for (int t = 0; t < MAXJ; ++t) dot[t] = fmaf(qc, kj[t][c], dot[t]);
+          for (int t = 0; t < MAXJ; ++t) acc[t] = fmaf(qc, kj[t][c], acc[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < MAXJ; ++t) dot[t] = c0 == 0 ? acc[t] : dot[t] + acc[t];
       }
     }
     float val[MAXJ];
@@ -260,54 +353,8 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
       }
       val[t] = a;
     }
-    if (LOCAL_K && g.off_aff && R <= 64 && g.topk > 4) {
-      // small grids, many routed regions: the rank of each of the lane's values in the row
-      // (larger values first, equal values by lower column) is its place in
-      // the top-k; one broadcast load per column, no shuffles
-      int rank_of[MAXJ];
-#pragma unroll
-      for (int t = 0; t < MAXJ; ++t) rank_of[t] = 0;
-      for (int jj = 0; jj < R; ++jj) {
-        float a = arow[s * R + jj];
-        a = (a == a) ? a : -INFINITY;
-#pragma unroll
-        for (int t = 0; t < MAXJ; ++t) {
-          const int j = lane + 32 * t;
-          rank_of[t] += (a > val[t] || (a == val[t] && jj < j)) ? 1 : 0;
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < MAXJ; ++t) {
-        const int j = lane + 32 * t;
-        if (j < R && rank_of[t] < g.topk) idx[((size_t)b * R + i) * g.topk + rank_of[t]] = j;
-      }
-      continue;
-    }
-    unsigned taken = 0;  // bit t: column lane + 32 t already chosen
-    for (int m = 0; m < g.topk; ++m) {
-      float bv = -INFINITY;
-      int bj = 0x7fffffff;
-#pragma unroll
-      for (int t = 0; t < MAXJ; ++t) {
-        const int j = lane + 32 * t;
-        if (j < R && !((taken >> t) & 1u) &&
-            (val[t] > bv || (val[t] == bv && j < bj))) {
-          bv = val[t];
-          bj = j;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
-        if (ov > bv || (ov == bv && oj < bj)) {
-          bv = ov;
-          bj = oj;
-        }
-      }
-      if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
-      if (lane == 0) idx[((size_t)b * R + i) * g.topk + m] = bj;
-    }
+    select_topk<MAXJ>(val, (LOCAL_K && g.off_aff) ? arow + s * R : nullptr, R, g.topk, lane,
+                      idx + ((size_t)b * R + i) * g.topk, nullptr);
   }
   if (!LOCAL_K) cluster.sync();  // keep km alive until every peer is done
 }
