@@ -370,6 +370,11 @@ class Setup:
         self.bra.attend(q, k, v, idx, self.wl.heads, self.wl.S, self.w, self.b, out=out,
                         stream=self.stream)
 
+    def attend_tc(self, s):
+        q, k, v, out, idx = self.bufs[s % self.sets]
+        self.bra.attend_tc(q, k, v, idx, self.wl.heads, self.wl.S, self.w, self.b, out=out,
+                           stream=self.stream)
+
     def capture(self, launch):
         """One CUDA graph per input set (launch overhead off the step)."""
         torch = self.torch
@@ -468,6 +473,12 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
     route_ms = st.time_kernel(st.route, kernel_steps)
     attend_ms = st.time_kernel(st.attend, kernel_steps)
     fwd_ms = st.time_kernel(st.fwd, kernel_steps)
+    # the tcgen05 formulation of the attend step, where its shape applies
+    # (8 x 8 regions, 64 channels, top-k <= 4)
+    tc_ms = None
+    if (wl.dtype == "bf16" and wl.C == 64 and wl.heads == 2 and wl.H // wl.S == 8
+            and wl.W // wl.S == 8 and wl.topk <= 4 and wl.ks in (1, 3, 5)):
+        tc_ms = st.time_kernel(st.attend_tc, kernel_steps)
     work = algorithmic_work(wl)
     ok = st.bra.device_status(stream)
     launches = st.launches()
@@ -480,6 +491,9 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
              "step_roofline": roofline(work["forward"], pk, wl.dtype, ms * 1e-3),
              "route_roofline": roofline(work["route"], pk, wl.dtype, route_ms * 1e-3),
              "attend_roofline": roofline(work["attend"], pk, wl.dtype, attend_ms * 1e-3),
+             **({"attend_tc_us": tc_ms * 1e3,
+                 "attend_tc_roofline": roofline(work["attend"], pk, wl.dtype, tc_ms * 1e-3)}
+                if tc_ms is not None else {}),
              "device_status": ok}
     if not no_cpu:
         cores = os.cpu_count() or 1

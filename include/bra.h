@@ -103,6 +103,22 @@ int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
                void *out, void *stream);
 
 /*
+ * bra_attend_tc -- bra_attend computed with the 5th-generation tensor cores
+ * (tcgen05.mma, accumulators in tensor memory) for maps of 8 x 8 regions with
+ * C = 64 (2 heads of 32), topk <= 4 and lepe_ks 1, 3 or 5: S = Q K^T for both
+ * heads at once against a block-diagonal Q operand (M = 128), P V block by
+ * block, the softmax and LePE on separate warps. Arguments, layout and errors
+ * as bra_attend; other shapes return BRA_ERR_UNSUPPORTED. The result equals
+ * bra_attend's within the bf16 tolerance (the exponentials and row sums are
+ * formed in the same precision; the order of additions differs). On the
+ * B300 this variant is measured slower than bra_attend for the stage-1 and
+ * 512 x 512 shapes, so bra_forward does not use it.
+ */
+int bra_attend_tc(const void *q, const void *k, const void *v, const int32_t *idx, int B,
+                  int H, int W, int C, int heads, int S, int topk, const float *lepe_w,
+                  const float *lepe_b, int lepe_ks, int dtype, void *out, void *stream);
+
+/*
  * bra_forward -- the whole forward: the routing of bra_route, then the
  * attention of bra_attend, on one stream.
  *   idx_workspace  device buffer of bra_idx_workspace_bytes(B, S, topk)

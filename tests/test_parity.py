@@ -35,6 +35,7 @@ SMALL = [
     Workload("tall_region_bf16", 1, 40, 8, 64, 2, 4, 3, 5, "bf16"),
     Workload("grid32_bf16", 1, 64, 64, 64, 2, 32, 2, 5, "bf16"),
     Workload("n16_c128_bf16", 3, 28, 28, 128, 4, 7, 4, 5, "bf16"),
+    Workload("n64_top3_many_units_bf16", 1, 128, 128, 64, 2, 16, 3, 5, "bf16"),
     Workload("ragged_n15_region_bf16", 1, 36, 60, 64, 2, 12, 3, 5, "bf16"),
     Workload("topk40_serial_copies_bf16", 1, 32, 32, 64, 2, 8, 40, 5, "bf16"),
     Workload("image_ks3_bf16", 3, 12, 12, 64, 2, 4, 5, 3, "bf16"),
@@ -175,3 +176,37 @@ def test_one_launch_forward_equals_two_kernel_forward(cuda_device):
     assert bra.device_status() == bra.BRA_OK
     assert torch.equal(idx_two, idx_big[:2])
     assert torch.equal(out_two, out_big[:2])
+
+
+TC_SHAPES = [
+    Workload("tc_n64_top2", 3, 16, 16, 64, 2, 2, 2, 5, "bf16"),
+    Workload("tc_top4_ks3", 1, 16, 16, 64, 2, 2, 4, 3, "bf16"),
+    Workload("tc_top3_many_units", 1, 128, 128, 64, 2, 16, 3, 5, "bf16"),
+    Workload("tc_one_region_ks1", 2, 8, 8, 64, 2, 1, 1, 1, "bf16"),
+]
+
+
+@pytest.mark.parametrize("wl", TC_SHAPES + [bra_synth.WORKLOADS["stage1_bf16"],
+                                            bra_synth.WORKLOADS["seg512_bf16"]],
+                         ids=lambda w: w.name)
+def test_tensor_memory_attend_matches_oracle(wl, cuda_device):
+    """bra_attend_tc (tcgen05.mma, accumulators in tensor memory) against the
+    oracle on the routing of bra_route, element by element."""
+    x = bra_synth.make_inputs(wl, seed=9)
+    q, k, v, w, b = device_inputs(wl, x, cuda_device)
+    idx = bra.route(q, k, wl.S, wl.topk)
+    out = bra.attend_tc(q, k, v, idx, wl.heads, wl.S, w, b)
+    assert bra.device_status() == bra.BRA_OK
+    ref = oracle.attend(x.q, x.k, x.v, idx.cpu().numpy(), wl.heads, wl.S, x.lepe_w, x.lepe_b,
+                        threads=8)
+    err = np.abs(out.float().cpu().numpy() - ref).max()
+    assert err <= TOL["bf16"], err
+
+
+def test_tensor_memory_attend_rejects_other_shapes(cuda_device):
+    q = torch.zeros((1, 28, 28, 128), dtype=torch.bfloat16, device=cuda_device)
+    idx = torch.zeros((1, 49, 4), dtype=torch.int32, device=cuda_device)
+    w = torch.zeros((128, 5, 5), device=cuda_device)
+    with pytest.raises(bra.BraError) as e:
+        bra.attend_tc(q, q.clone(), q.clone(), idx, 4, 7, w)
+    assert e.value.status == bra.BRA_ERR_UNSUPPORTED

@@ -14,7 +14,7 @@ import os
 
 import torch
 
-__all__ = ["BraError", "route", "attend", "forward", "forward_static", "forward_host",
+__all__ = ["BraError", "route", "attend", "attend_tc", "forward", "forward_static", "forward_host",
            "HostPipeline",
            "idx_workspace_bytes", "forward_launches", "device_status", "check_wait_timeout", "library_path",
            "SYMBOLS"]
@@ -30,6 +30,7 @@ _P, _I = ctypes.c_void_p, ctypes.c_int
 SYMBOLS = {
     "bra_route": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "bra_attend": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
+    "bra_attend_tc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "bra_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
     "bra_forward_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "bra_idx_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
@@ -140,6 +141,19 @@ def attend(q, k, v, idx, heads: int, S: int, lepe_w, lepe_b=None, out=None, stre
                             topk, _ptr(lepe_w), _ptr(lepe_b), lepe_w.shape[-1],
                             _dtype_code(q), _ptr(out), _stream(stream))
     _check(rc, "bra_attend")
+    return out
+
+
+def attend_tc(q, k, v, idx, heads: int, S: int, lepe_w, lepe_b=None, out=None, stream=None):
+    """bra_attend on the tcgen05 tensor cores (8 x 8 regions, C = 64, topk <= 4)."""
+    B, H, W, C = _map(q, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    topk = idx.shape[-1]
+    rc = _load().bra_attend_tc(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), B, H, W, C, heads, S,
+                               topk, _ptr(lepe_w), _ptr(lepe_b), lepe_w.shape[-1],
+                               _dtype_code(q), _ptr(out), _stream(stream))
+    _check(rc, "bra_attend_tc")
     return out
 
 

@@ -565,6 +565,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
     }
   }
   if (grp < groups && gw == kGroupWarps - 1 && lane < g.nc) tma_store_wait_read();
+  if (tid == 0) settle_after_timeout();
 }
 
 }  // namespace bra

@@ -1,0 +1,532 @@
+// attend_tc.cuh -- fused routed attention + LePE on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory) for bf16 maps with 8 x 8
+// regions (64 tokens), 64 channels (2 heads of 32) and up to 4 routed regions
+// per query region: the BiFormer stage-1 shape and the 512 x 512 dense-
+// prediction shape.
+//
+// Same operation as attend_bf16.cuh (page "CVPR2023：BiFormer中的双层路由
+// 注意力机制解析" §3: k_g = gather(k, I_r), attn = softmax(q k_g^T * scale),
+// out = attn v_g, out += lce(v); LePE of page "从静态到动态：BRA双层路由注意力
+// 如何革新视觉Transformer的计算范式" §4; page "BiFormer: Vision Transformer mit
+// Bi-Level-Routing-Attention": attention over the union of the routed
+// regions, with dense matrix products only).
+//
+// One persistent CTA of 16 warps per SM walks the query regions ("units")
+// blockIdx.x, blockIdx.x + gridDim.x, ... . The warps have roles:
+//   warp 0     copies each unit's Q tile (TMA box) into a Q ring, one unit
+//              ahead, and turns the landed tile into a block-diagonal 128 x 64
+//              operand: rows 0-63 hold head 0's queries with channels 32-63
+//              zero, rows 64-127 head 1's with channels 0-31 zero, so that one
+//              M = 128 MMA computes both heads' logits against one K tile;
+//   warp 1     one thread issues S = Q_bd K^T (M = 128, N = 64 topk, K = 64)
+//              into a tensor-memory slot and O = P V block by block (M = 128,
+//              N = 64, K = 64 keys per block) into the slot's first 64
+//              columns, whichever has its inputs first;
+//   warp 2     copies each unit's V halo (region plus ks/2 border, zero filled
+//              outside the image) into a halo ring;
+//   warp 3     reads the routing and copies the routed regions' K and V tiles
+//              by index into a K ring and a V ring;
+//   warps 4-7  own the 128 tensor-memory lanes (row r: head r / 64, query
+//              r % 64): the row maximum of S, P = 2^(S d^-1/2 log2 e - max) as
+//              bf16 (the operand of P V) into shared memory 64 keys at a time,
+//              the row sum of that bf16 P in f32; then, after the next unit's
+//              softmax, O / sum plus the LePE from the O tile, rounded once to
+//              bf16 into a staging tile that one thread stores with a TMA copy;
+//   warps 8-15 the LePE stencil of each unit from the halo, ahead of the
+//              tensor cores, into an f32 O tile.
+// Only warp 3 reads the routing index, so when the kernel is launched right
+// after the routing grid (programmatic dependent launch) everything else --
+// Q tiles, halos, LePE -- starts before that grid has finished. Every ring,
+// slot and tile hand-off is an mbarrier, every wait bounded. The operand
+// layouts are those of tcgen05.cuh (128-byte swizzled rows).
+#pragma once
+
+#include "attend_bf16.cuh"
+#include "tcgen05.cuh"
+
+namespace bra {
+
+constexpr int kTcWarps = 20;
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr int kTcLepeThreads = 256;   // warps 12-19
+constexpr int kTcLepeWarp0 = 12;
+constexpr uint32_t kTcTmemCols = 512;
+
+struct TcGeom {
+  int H, W, S, topk, R, units;
+  int nh, nk, nv;           // halo, K and V ring stages (halo <= 4, K and V <= 2)
+  int nslot;                // tensor-memory slots (<= 4)
+  uint32_t slot_cols;       // columns of a slot (>= 64 topk, a power of two)
+  int halo_w, halo_h;
+  uint32_t off_h, off_k, off_v, off_ones, off_p, off_o, off_st, off_w, off_bar;  // Q ring at 0
+  int sum_mma;              // row sums from the P V MMA (one key block): N = 80, the
+                            // 16 extra columns against a tile of ones
+  uint32_t h_bytes;         // bytes of one halo stage
+  float scale_log2;         // d^-1/2 * log2(e)
+};
+
+// Barrier slots (uint64 each) from off_bar; rings of up to four.
+enum TcBar {
+  kBarFq = 0,       // [2] Q tile landed (TMA)
+  kBarQready = 2,   // [2] block-diagonal Q built (1 arrival)
+  kBarQfree = 4,    // [2] Q operand read (MMA commit)
+  kBarFh = 6,       // [4] halo landed (TMA)
+  kBarHfree = 10,   // [4] halo read (256 LePE arrivals)
+  kBarFk = 14,      // [2] K tiles landed (TMA)
+  kBarKfree = 16,   // [2] K tiles read (MMA commit)
+  kBarFv = 18,      // [2] V tiles landed (TMA)
+  kBarVfree = 20,   // [2] V tiles read (MMA commit)
+  kBarSfull = 22,   // [4] S in a tensor-memory slot (MMA commit)
+  kBarOfull = 26,   // [4] O in a tensor-memory slot (MMA commit)
+  kBarTfree = 30,   // [4] slot read (128 arrivals)
+  kBarPfull = 34,   // [2] P block of softmax warpgroup g written (128 arrivals)
+  kBarPfree = 36,   // [2] P block of softmax warpgroup g read (MMA commit)
+  kBarOfill = 38,   // [2] LePE written into the O tile (256 arrivals)
+  kBarOfree = 40,   // [2] O tile consumed and stored (128 arrivals)
+  kBarDone = 42,    // every MMA complete (MMA commit), before the tensor memory is freed
+  kBarCount = 43
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Parity to wait for on a "full" barrier at the n-th use of its ring slot,
+// and on a "free" barrier (the first use of a slot does not wait: a fresh
+// barrier's preceding phase counts as complete).
+__device__ __forceinline__ uint32_t full_parity(int n) { return (uint32_t)(n & 1); }
+__device__ __forceinline__ uint32_t free_parity(int n) { return (uint32_t)((n & 1) ^ 1); }
+
+template <int KS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    bra_attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_vh,
+                         const __grid_constant__ CUtensorMap tm_o,
+                         const int32_t *__restrict__ idx, const float *__restrict__ lepe_w,
+                         const float *__restrict__ lepe_b, TcGeom g) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t *smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
+  float *sw = reinterpret_cast<float *>(smem + g.off_w);  // [KS*KS][64], bias [64]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + g.off_bar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBarCount);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int PAD = KS / 2;
+  const int topk = g.topk;
+  const int n_units = g.units > (int)blockIdx.x
+                          ? (g.units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+                          : 0;
+
+  // ---- set-up: barriers, weights, the permanent zeros of the Q operands
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kBarFq + i], 1);
+      mbar_init(&bars[kBarQready + i], 1);
+      mbar_init(&bars[kBarQfree + i], 1);
+      mbar_init(&bars[kBarFk + i], 1);
+      mbar_init(&bars[kBarKfree + i], 1);
+      mbar_init(&bars[kBarFv + i], 1);
+      mbar_init(&bars[kBarVfree + i], 1);
+      mbar_init(&bars[kBarPfull + i], 128);
+      mbar_init(&bars[kBarPfree + i], 1);
+      mbar_init(&bars[kBarOfill + i], kTcLepeThreads);
+      mbar_init(&bars[kBarOfree + i], 128);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[kBarFh + i], 1);
+      mbar_init(&bars[kBarHfree + i], kTcLepeThreads);
+      mbar_init(&bars[kBarSfull + i], 1);
+      mbar_init(&bars[kBarOfull + i], 1);
+      mbar_init(&bars[kBarTfree + i], 128);
+    }
+    mbar_init(&bars[kBarDone], 1);
+    fence_mbar_init();
+  }
+  for (int e = tid; e < 64 * KS * KS; e += kTcThreads) {
+    const int tap = e / 64, c = e % 64;
+    sw[e] = __ldg(lepe_w + (size_t)c * KS * KS + tap);
+  }
+  if (tid < 64) sw[KS * KS * 64 + tid] = lepe_b ? __ldg(lepe_b + tid) : 0.f;
+  // the ones tile (bf16 1.0), the extra N columns of P V that give row sums
+  if (g.sum_mma)
+    for (int e = tid; e < 8192 / 16; e += kTcThreads)
+      *reinterpret_cast<uint4 *>(smem + g.off_ones + e * 16) =
+          make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+  // rows 64-127, chunks 0-3 of both Q operands stay zero
+  for (int e = tid; e < 2 * 64 * 4; e += kTcThreads) {
+    const int st = e >> 8, r = 64 + ((e >> 2) & 63), c = e & 3;
+    *reinterpret_cast<uint4 *>(smem + st * 16384 + swz128(r, c)) = make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTcTmemCols);
+    tmem_relinquish();
+  }
+  fence_async_shared();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto unit_at = [&](int k, int &b, int &y0, int &x0) {
+    const int u = blockIdx.x + k * gridDim.x;
+    const int i = u % g.R;
+    b = u / g.R;
+    y0 = (i / g.S) * 8;
+    x0 = (i % g.S) * 8;
+  };
+
+  if (warp == 0) {
+    // ============================================= Q tiles and Q_bd builds
+    if (lane == 0) prefetch_tensormap(&tm_q);
+    auto issue_q = [&](int k) {
+      const int st = k & 1;
+      mbar_wait(&bars[kBarQfree + st], free_parity(k >> 1));
+      if (lane == 0) {
+        int b, y0, x0;
+        unit_at(k, b, y0, x0);
+        mbar_arrive_expect_tx(&bars[kBarFq + st], 8192);
+        tma_load_4d(smem + st * 16384, &tm_q, &bars[kBarFq + st], 0, x0, y0, b);
+      }
+      __syncwarp();
+    };
+    if (n_units > 0) issue_q(0);
+    for (int k = 0; k < n_units; ++k) {
+      if (k + 1 < n_units) issue_q(k + 1);
+      const int st = k & 1;
+      mbar_wait(&bars[kBarFq + st], full_parity(k >> 1));
+      // chunks 4-7 (head 1's channels) of rows 0-63 move to rows 64-127 (the
+      // same swizzled positions: a row and the row 64 below share r % 8)
+      uint8_t *a = smem + st * 16384;
+#pragma unroll
+      for (int e = lane; e < 256; e += 32) {
+        const int r = e >> 2, c = 4 + (e & 3);
+        uint4 *src = reinterpret_cast<uint4 *>(a + swz128(r, c));
+        *reinterpret_cast<uint4 *>(a + swz128(r + 64, c)) = *src;
+        *src = make_uint4(0, 0, 0, 0);
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarQready + st]);
+    }
+    // no Q copy still in flight at exit (they were all waited for above,
+    // unless a wait gave up)
+    for (int k = (n_units > 2 ? n_units - 2 : 0); k < n_units; ++k)
+      mbar_drain(&bars[kBarFq + (k & 1)], full_parity(k >> 1));
+  } else if (warp == 1) {
+    // ====================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, 64 * topk, 0);
+      const uint32_t idesc_o = idesc_bf16_f32(128, g.sum_mma ? 80 : 64, 1);
+      int next1 = 0;           // next unit for S = Q_bd K^T
+      int next2 = 0, blk = 0;  // next unit and key block for O = P V
+      int pcnt[2] = {0, 0};    // P blocks consumed so far from each warpgroup's buffer
+      uint64_t t_idle = 0;
+      while (next2 < n_units) {
+        bool progressed = false;
+        // S of the next unit, as soon as its Q operand, K tiles and slot are ready
+        if (next1 < n_units) {
+          const int k = next1, qs = k & 1, ks_ = k % g.nk, sl = k % g.nslot;
+          if (mbar_try_wait(&bars[kBarQready + qs], full_parity(k >> 1)) &&
+              mbar_try_wait(&bars[kBarFk + ks_], full_parity(k / g.nk)) &&
+              mbar_try_wait(&bars[kBarTfree + sl], free_parity(k / g.nslot))) {
+            tc_fence_after();
+            const uint32_t d = tmem + sl * g.slot_cols;
+            const uint32_t a0 = smem_u32(smem + qs * 16384);
+            const uint32_t k0 = smem_u32(smem + g.off_k + ks_ * topk * 8192);
+            for (int s = 0; s < 4; ++s)
+              mma_bf16_ss(d, smem_desc_sw128(a0 + 32 * s, 1024),
+                          smem_desc_sw128(k0 + 32 * s, 1024), idesc_s, s > 0);
+            mma_commit(&bars[kBarSfull + sl]);
+            mma_commit(&bars[kBarQfree + qs]);
+            mma_commit(&bars[kBarKfree + ks_]);
+            ++next1;
+            progressed = true;
+          }
+        }
+        // the next P block of the oldest unit whose S is out, once written
+        if (next2 < next1) {
+          const int k = next2, pb = k & 1, vs = k % g.nv, sl = k % g.nslot;
+          if (mbar_try_wait(&bars[kBarPfull + pb], full_parity(pcnt[pb])) &&
+              (blk > 0 || mbar_try_wait(&bars[kBarFv + vs], full_parity(k / g.nv)))) {
+            tc_fence_after();
+            const uint32_t d = tmem + sl * g.slot_cols;
+            const uint32_t p0 = smem_u32(smem + g.off_p + pb * 16384);
+            const uint32_t v0 = smem_u32(smem + g.off_v + vs * topk * 8192) + blk * 8192;
+            const uint32_t lbo = smem_u32(smem + g.off_ones) - v0;  // V atom -> ones atom
+            for (int s = 0; s < 4; ++s)
+              mma_bf16_ss(d, smem_desc_sw128(p0 + 32 * s, 1024),
+                          smem_desc_sw128_lbo(v0 + s * 2048, g.sum_mma ? lbo : 0u, 1024),
+                          idesc_o, (blk > 0 || s > 0) ? 1u : 0u);
+            mma_commit(&bars[kBarPfree + pb]);
+            ++pcnt[pb];
+            if (++blk == topk) {
+              mma_commit(&bars[kBarOfull + sl]);
+              mma_commit(&bars[kBarVfree + vs]);
+              blk = 0;
+              ++next2;
+            }
+            progressed = true;
+          }
+        }
+        // give up (and flag it) if nothing moves for as long as a bounded wait
+        if (progressed) {
+          t_idle = 0;
+        } else if (t_idle == 0) {
+          t_idle = global_ns();
+        } else if (global_ns() - t_idle > kWaitLimitNs ||
+                   (*reinterpret_cast<volatile unsigned *>(&g_status) & kStatusTimeout)) {
+          atomicOr(&g_status, kStatusTimeout);
+          break;
+        }
+      }
+      mma_commit(&bars[kBarDone]);
+      mbar_drain(&bars[kBarDone], 0);  // every MMA complete before the memory is freed
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ================================================= halo producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_vh);
+      for (int k = 0; k < n_units; ++k) {
+        const int st = k % g.nh;
+        mbar_wait(&bars[kBarHfree + st], free_parity(k / g.nh));
+        int b, y0, x0;
+        unit_at(k, b, y0, x0);
+        mbar_arrive_expect_tx(&bars[kBarFh + st], g.h_bytes);
+        tma_load_4d(smem + g.off_h + st * g.h_bytes, &tm_vh, &bars[kBarFh + st], 0, x0 - PAD,
+                    y0 - PAD, b);
+      }
+      // no halo copy still in flight at exit
+      for (int k = (n_units > g.nh ? n_units - g.nh : 0); k < n_units; ++k)
+        mbar_drain(&bars[kBarFh + k % g.nh], full_parity(k / g.nh));
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ================================================ K and V producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+    }
+    grid_dependency_wait();  // the routing index comes from the previous grid
+    for (int k = 0; k < n_units; ++k) {
+      const int u = blockIdx.x + k * gridDim.x;
+      const int b = u / g.R;
+      const int ks_ = k % g.nk, vs = k % g.nv;
+      const int j = lane < topk ? __ldg(idx + (size_t)u * topk + lane) : 0;
+      // lanes 0..topk-1: K of routed region lane; lanes 4..4+topk-1: its V
+      const int m = lane & 3;
+      const int jm = __shfl_sync(0xffffffffu, j, m);
+      const bool is_v = lane >= 4;
+      const bool active = lane < 8 && m < topk;
+      int xj = 0, yj = g.H;  // a box wholly below the image is all fill (zeros)
+      if (jm < 0 || jm >= g.R) {
+        if (active && !is_v) atomicOr(&g_status, kStatusBadIndex);
+      } else {
+        xj = (jm % g.S) * 8;
+        yj = (jm / g.S) * 8;
+      }
+      mbar_wait(&bars[kBarKfree + ks_], free_parity(k / g.nk));
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFk + ks_], topk * 8192);
+      __syncwarp();
+      if (active && !is_v)
+        tma_load_4d(smem + g.off_k + (ks_ * topk + m) * 8192, &tm_k, &bars[kBarFk + ks_], 0, xj,
+                    yj, b);
+      mbar_wait(&bars[kBarVfree + vs], free_parity(k / g.nv));
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFv + vs], topk * 8192);
+      __syncwarp();
+      if (active && is_v)
+        tma_load_4d(smem + g.off_v + (vs * topk + m) * 8192, &tm_v, &bars[kBarFv + vs], 0, xj,
+                    yj, b);
+    }
+    // no K or V copy still in flight at exit
+    for (int k = (n_units > g.nk ? n_units - g.nk : 0); k < n_units; ++k)
+      mbar_drain(&bars[kBarFk + k % g.nk], full_parity(k / g.nk));
+    for (int k = (n_units > g.nv ? n_units - g.nv : 0); k < n_units; ++k)
+      mbar_drain(&bars[kBarFv + k % g.nv], full_parity(k / g.nv));
+  } else if (warp < kTcLepeWarp0) {
+    // ========================== softmax and O epilogue (TMEM lanes), two
+    // warpgroups taking alternate units
+    const int wg = (warp - 4) >> 2;  // 0: warps 4-7, 1: warps 8-11
+    const int r = (tid - 128) & 127;  // tensor-memory lane = operand row
+    const int h = r >> 6, tq = r & 63;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const float2 sc2 = make_float2(g.scale_log2, g.scale_log2);
+    int pcnt = 0;  // P blocks this warpgroup has written (into its own buffer)
+    float inv_prev = 0.f;
+    // O of unit k (in its slot, once out) / row sum, plus the LePE that the
+    // LePE warps left in the O tile, rounded once to bf16 into the staging
+    // tile, which one thread stores with a TMA copy
+    auto epilogue = [&](int k, float inv) {
+      const int sl = k % g.nslot, ot = k & 1;
+      mbar_wait(&bars[kBarOfull + sl], full_parity(k / g.nslot));
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld32(lane_base + sl * g.slot_cols + h * 32, v);
+      if (g.sum_mma) inv = __uint_as_float(tmem_ld1(lane_base + sl * g.slot_cols + 64));
+      tmem_ld_wait();
+      if (g.sum_mma) inv = 1.f / inv;
+      tc_fence_before();
+      mbar_arrive(&bars[kBarTfree + sl]);
+      mbar_wait(&bars[kBarOfill + ot], full_parity(k >> 1));
+      // this warpgroup's previous store (from the same staging tile) has been read
+      if (r == 0) tma_store_wait_read();
+      named_sync(3 + wg, 128);
+      // O tile [64 tokens][16 chunks of 4 floats]: chunk c of token t sits at
+      // chunk position c ^ (t % 8); staging tile [64 tokens][8 chunks of 8
+      // bf16], 128-byte swizzled (chunk c at c ^ (t % 8)), as the store's
+      // tensor map expects
+      const float *orow =
+          reinterpret_cast<const float *>(smem + g.off_o + ot * 16384) + tq * 64 + h * 32;
+      uint8_t *srow_st = smem + g.off_st + ot * 8192 + tq * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 8 channels a step: O chunks 2c, 2c + 1
+        const float4 l0 = *reinterpret_cast<const float4 *>(orow + (((2 * c) ^ (tq & 7)) << 2));
+        const float4 l1 =
+            *reinterpret_cast<const float4 *>(orow + (((2 * c + 1) ^ (tq & 7)) << 2));
+        const uint4 packed = make_uint4(
+            pack_bf16x2(fmaf(__uint_as_float(v[8 * c]), inv, l0.x),
+                        fmaf(__uint_as_float(v[8 * c + 1]), inv, l0.y)),
+            pack_bf16x2(fmaf(__uint_as_float(v[8 * c + 2]), inv, l0.z),
+                        fmaf(__uint_as_float(v[8 * c + 3]), inv, l0.w)),
+            pack_bf16x2(fmaf(__uint_as_float(v[8 * c + 4]), inv, l1.x),
+                        fmaf(__uint_as_float(v[8 * c + 5]), inv, l1.y)),
+            pack_bf16x2(fmaf(__uint_as_float(v[8 * c + 6]), inv, l1.z),
+                        fmaf(__uint_as_float(v[8 * c + 7]), inv, l1.w)));
+        *reinterpret_cast<uint4 *>(srow_st + (((h * 4 + c) ^ (tq & 7)) << 4)) = packed;
+      }
+      fence_async_shared();
+      named_sync(3 + wg, 128);
+      if (r == 0) {
+        int b, y0, x0;
+        unit_at(k, b, y0, x0);
+        tma_store_4d(&tm_o, smem + g.off_st + ot * 8192, 0, x0, y0, b);
+        tma_store_commit();
+      }
+      mbar_arrive(&bars[kBarOfree + ot]);
+    };
+    for (int k = wg; k < n_units; k += 2) {
+      const int sl = k % g.nslot;
+      const uint32_t srow = lane_base + sl * g.slot_cols;
+      mbar_wait(&bars[kBarSfull + sl], full_parity(k / g.nslot));
+      tc_fence_after();
+      // the row maximum of the raw logits (four independent chains), 32
+      // columns at a time
+      uint32_t v[32];
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      for (int c0 = 0; c0 < 64 * topk; c0 += 32) {
+        tmem_ld32(srow + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          m4[0] = max3(m4[0], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+          m4[1] = max3(m4[1], __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+          m4[2] = max3(m4[2], __uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
+          m4[3] = max3(m4[3], __uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
+        }
+      }
+      const float base = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * g.scale_log2;
+      const float2 nb = make_float2(-base, -base);
+      // P (bf16) 64 keys at a time into this warpgroup's P buffer, and its
+      // row sum (four chains) unless the MMA forms it
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int blk = 0; blk < topk; ++blk, ++pcnt) {
+        mbar_wait(&bars[kBarPfree + wg], free_parity(pcnt));
+        uint8_t *prow = smem + g.off_p + wg * 16384 + r * 128;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(srow + blk * 64 + half * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // 16-byte chunk half*4 + c: 8 keys
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 8 * c + 2 * e;
+              const float2 x = __ffma2_rn(
+                  make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sc2, nb);
+              pk[e] = exp2_bf16x2(x.x, x.y);
+              if (!g.sum_mma) l4[e] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+            }
+            *reinterpret_cast<uint4 *>(prow + (((half * 4 + c) ^ (r & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+        fence_async_shared();
+        tc_fence_before();
+        mbar_arrive(&bars[kBarPfull + wg]);
+      }
+      const float inv = 1.f / ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+      if (g.nslot >= 4) {
+        // this warpgroup's previous unit (its O is out by now: its P V was
+        // issued before this unit's P was written); its slot is not the one
+        // the warpgroup's next unit needs
+        if (k >= 2) epilogue(k - 2, inv_prev);
+        inv_prev = inv;
+      } else {
+        // two slots: each warpgroup owns one, so its next unit's S can only
+        // be formed once this unit's O has been read
+        epilogue(k, inv);
+      }
+    }
+    if (g.nslot >= 4) {  // the last unit of this warpgroup
+      const int last = n_units - 1 - ((n_units - 1 - wg) & 1);
+      if (last >= wg) epilogue(last, inv_prev);
+    }
+    if (r == 0) tma_store_wait_read();
+  } else {
+    // ======================================== LePE, O add, output store
+    const int lt = tid - 32 * kTcLepeWarp0;  // 0..255
+    const int cp = lt & 31, x = lt >> 5;     // channel pair, column of the region
+    const int c = 2 * cp;
+    float2 wgt[KS * KS];
+#pragma unroll
+    for (int e = 0; e < KS * KS; ++e) wgt[e] = *reinterpret_cast<const float2 *>(sw + e * 64 + c);
+    const float2 bias = *reinterpret_cast<const float2 *>(sw + KS * KS * 64 + c);
+    for (int k = 0; k < n_units; ++k) {
+      const int hs = k % g.nh, ot = k & 1;
+      mbar_wait(&bars[kBarFh + hs], full_parity(k / g.nh));
+      const uint8_t *hb = smem + g.off_h + hs * g.h_bytes;
+      float2 acc[8];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) acc[rr] = bias;
+      const uint8_t *col = hb + x * 128 + c * 2;
+#pragma unroll
+      for (int yy = 0; yy < 8 + KS - 1; ++yy) {
+        const uint8_t *rp = col + yy * (8 + KS - 1) * 128;
+#pragma unroll
+        for (int w = 0; w < KS; ++w) {
+          const uint32_t t2 = *reinterpret_cast<const uint32_t *>(rp + w * 128);
+          const float2 vv = make_float2(__uint_as_float(__byte_perm(t2, 0u, 0x1044u)),
+                                        __uint_as_float(__byte_perm(t2, 0u, 0x3244u)));
+#pragma unroll
+          for (int uu = 0; uu < KS; ++uu) {
+            const int rr = yy - uu;
+            if (rr >= 0 && rr < 8) acc[rr] = __ffma2_rn(wgt[uu * KS + w], vv, acc[rr]);
+          }
+        }
+      }
+      mbar_arrive(&bars[kBarHfree + hs]);  // the halo is no longer read
+      // the LePE (f32) into the O tile, where the epilogue adds O
+      mbar_wait(&bars[kBarOfree + ot], free_parity(k >> 1));
+      float *otile = reinterpret_cast<float *>(smem + g.off_o + ot * 16384);
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const int t = rr * 8 + x;
+        *reinterpret_cast<float2 *>(otile + t * 64 + (((c >> 2) ^ (t & 7)) << 2) + (c & 3)) =
+            acc[rr];
+      }
+      mbar_arrive(&bars[kBarOfill + ot]);
+    }
+  }
+
+  // ---- tear-down: every MMA has completed (warp 1 waited for that)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTcTmemCols);
+  if (tid == 0) settle_after_timeout();
+}
+
+}  // namespace bra

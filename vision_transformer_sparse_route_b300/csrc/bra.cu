@@ -17,6 +17,7 @@
 #include "attend_bf16.cuh"
 #include "attend_f32.cuh"
 #include "attend_image.cuh"
+#include "attend_tc.cuh"
 #include "forward_image.cuh"
 #include "route.cuh"
 
@@ -26,6 +27,7 @@ using bra::AttendF32Geom;
 using bra::AttendGeom;
 using bra::FusedGeom;
 using bra::ImageGeom;
+using bra::TcGeom;
 
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;
 
@@ -426,6 +428,51 @@ bool plan_attend_bf16(int B, int H, int W, int C, int heads, int S, int topk, in
   return *smem <= kMaxSmemPerBlock;
 }
 
+// The tensor-memory kernel: bf16, 8 x 8 regions, 64 channels (2 heads of
+// 32), at most 4 routed regions (N = 64 topk columns of a tensor-memory
+// slot), LePE kernel 1, 3 or 5. Ring depths are the deepest that fit in
+// shared memory: K and V rings of 2 (else 1), a halo ring of 3 (else 2).
+bool plan_attend_tc(int B, int H, int W, int C, int heads, int S, int topk, int ks,
+                    TcGeom *g, size_t *smem) {
+  if (C != 64 || heads != 2 || H / S != 8 || W / S != 8 || topk > 4) return false;
+  if (ks != 1 && ks != 3 && ks != 5) return false;
+  TcGeom a = {};
+  a.H = H; a.W = W; a.S = S; a.topk = topk; a.R = S * S;
+  a.units = B * a.R;
+  a.halo_w = a.halo_h = 8 + ks - 1;
+  a.h_bytes = (uint32_t)a.halo_w * a.halo_h * 128u;
+  // one key block: P V also forms the row sums (N = 80), so a slot needs 80
+  // columns
+  a.sum_mma = topk == 1;
+  a.slot_cols = a.sum_mma ? 128 : 64;
+  while (a.slot_cols < (uint32_t)(64 * topk)) a.slot_cols *= 2;
+  a.nslot = std::min(4, (int)(bra::kTcTmemCols / a.slot_cols));
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
+  const size_t w_bytes = (size_t)(ks * ks + 1) * 64 * 4;
+  const size_t bars = (size_t)bra::kBarCount * 8 + 16;
+  const size_t tile = (size_t)topk * 8192;  // K or V tiles of one unit
+  for (int nkv = 2; nkv >= 1; --nkv)
+    for (int nh = 3; nh >= 2; --nh) {
+      a.nk = a.nv = nkv;
+      a.nh = nh;
+      a.off_h = 2 * 16384;
+      a.off_k = (uint32_t)round_up((size_t)a.off_h + (size_t)nh * a.h_bytes, 1024);
+      a.off_v = (uint32_t)(a.off_k + nkv * tile);
+      a.off_ones = (uint32_t)(a.off_v + nkv * tile);
+      a.off_p = a.off_ones + (a.sum_mma ? 8192u : 0u);
+      a.off_o = a.off_p + 2 * 16384;
+      a.off_st = a.off_o + 2 * 16384;
+      a.off_w = a.off_st + 2 * 8192;
+      a.off_bar = (uint32_t)round_up(a.off_w + w_bytes, 8);
+      *smem = (size_t)a.off_bar + bars + 1024;  // slack to align the base to 1024 bytes
+      if (*smem <= kMaxSmemPerBlock) {
+        *g = a;
+        return true;
+      }
+    }
+  return false;
+}
+
 // The image-resident kernel: bf16, regions of fewer than 16 tokens (a 16-row
 // query block is then partly empty and a region's box copies are under 2 KB),
 // and one 64-channel chunk of the whole image's Q, K, V, V halo and f32 O in
@@ -564,6 +611,33 @@ int launch_attend_bf16_ks(const void *q, const void *k, const void *v,
     case 2: return launch_attend_bf16_kr<KS, 2, 0, 0>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
     default: return launch_attend_bf16_kr<KS, 1, 0, 0>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
   }
+}
+
+template <int KS>
+int launch_attend_tc_ks(const void *q, const void *k, const void *v, const int32_t *idx, int B,
+                        int C, const float *w, const float *bias, void *out, const TcGeom &g,
+                        size_t smem, bool pdl, cudaStream_t s) {
+  CUtensorMap tq, tk, tv, th, to;
+  if (!make_map(&tq, q, B, g.H, g.W, C, 8, 8, true) ||
+      !make_map(&tk, k, B, g.H, g.W, C, 8, 8, true) ||
+      !make_map(&tv, v, B, g.H, g.W, C, 8, 8, true) ||
+      !make_map(&th, v, B, g.H, g.W, C, g.halo_w, g.halo_h, false) ||
+      !make_map(&to, out, B, g.H, g.W, C, 8, 8, true))
+    return BRA_ERR_CUDA;
+  auto kern = bra::bra_attend_tc_kernel<KS>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min(g.units, sm_count()), 1, 1);
+  cfg.blockDim = dim3(bra::kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, th, to, idx, w, bias, g));
 }
 
 template <int KS, int RB>
@@ -845,6 +919,24 @@ int bra_forward(const void *q, const void *k, const void *v, int B, int H, int W
   (void)cudaGetLastError();
   return launch_forward(q, k, v, B, H, W, C, heads, S, topk, lepe_w, lepe_b, lepe_ks, dtype,
                         idx_workspace, out, static_cast<cudaStream_t>(stream));
+}
+
+int bra_attend_tc(const void *q, const void *k, const void *v, const int32_t *idx, int B,
+                  int H, int W, int C, int heads, int S, int topk, const float *lepe_w,
+                  const float *lepe_b, int lepe_ks, int dtype, void *out, void *stream) {
+  int rc = check_attend(q, k, v, idx, B, H, W, C, heads, S, topk, lepe_w, lepe_ks, dtype, out);
+  if (rc || B == 0) return rc;
+  TcGeom g;
+  size_t smem;
+  if (dtype != BRA_BF16 || !plan_attend_tc(B, H, W, C, heads, S, topk, lepe_ks, &g, &smem))
+    return BRA_ERR_UNSUPPORTED;
+  (void)cudaGetLastError();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (lepe_ks) {
+    case 1: return launch_attend_tc_ks<1>(q, k, v, idx, B, C, lepe_w, lepe_b, out, g, smem, false, s);
+    case 3: return launch_attend_tc_ks<3>(q, k, v, idx, B, C, lepe_w, lepe_b, out, g, smem, false, s);
+    default: return launch_attend_tc_ks<5>(q, k, v, idx, B, C, lepe_w, lepe_b, out, g, smem, false, s);
+  }
 }
 
 int bra_forward_launches(int B, int H, int W, int C, int heads, int S, int topk, int lepe_ks,

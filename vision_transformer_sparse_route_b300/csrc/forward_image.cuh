@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     const int x = rest % g.W, ry0 = (rest / g.W) * RB;
     image_lepe_item<KS, RB>(g, hb, so, gout, 2 * cp, x, ry0, sw);
   }
+  if (tid == 0) settle_after_timeout();
 }
 
 }  // namespace bra

@@ -84,6 +84,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   return true;
 }
 
+// Waits for phase `parity` of `bar` for at most limit_ns even after a wait of
+// this launch has given up: used before a CTA exits or frees memory, so that
+// no copy or MMA it issued is still in flight. Sets kStatusTimeout on giving up.
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity,
+                                           uint64_t limit_ns = kWaitLimitNs) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) {
+      atomicOr(&g_status, kStatusTimeout);
+      return false;
+    }
+  return true;
+}
+
+// Called by one thread at the very end of a kernel that issues TMA copies:
+// after a wait of this launch has given up, the normal hand-offs no longer
+// guarantee that every copy has landed, so the CTA stays alive a little
+// longer (its shared memory must outlive its copies).
+__device__ __forceinline__ void settle_after_timeout() {
+  if (*reinterpret_cast<volatile unsigned *>(&g_status) & kStatusTimeout) {
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 200000ull) {
+    }
+  }
+}
+
 // -------------------------------------------------------------------- TMA
 // 4-D tiled load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map,
