@@ -47,6 +47,7 @@ def _load():
             "oracle_lepe": [P, I, I, I, I, P, P, I, P],
             "oracle_attend": [P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, I],
             "oracle_forward": [P, P, P, I, I, I, I, I, I, I, P, P, I, P, P, I],
+            "oracle_qkv_project": [P, I, I, P, P, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -166,3 +167,19 @@ def forward(q, k, v, heads: int, S: int, topk: int, w, bias, threads: int = 1):
                                   _p(w), _p(bias), w.shape[-1], _p(idx), _p(out), threads),
            "forward")
     return out, idx
+
+
+def qkv_project(x, w, bias=None):
+    """(q, k, v) = the three C-column blocks of x W^T + bias, per token.
+    x [..., C]; w [3C, C]; bias [3C] or None. Returns float64 arrays of x's
+    shape."""
+    x, w = _f64(x), _f64(w)
+    bias = None if bias is None else _f64(bias)
+    C = x.shape[-1]
+    if w.shape != (3 * C, C):
+        raise ValueError("w must be [3C, C]")
+    M = int(np.prod(x.shape[:-1]))
+    q, k, v = (np.empty_like(x) for _ in range(3))
+    _check(_load().oracle_qkv_project(_p(x), M, C, _p(w), _p(bias), _p(q), _p(k), _p(v)),
+           "qkv_project")
+    return q, k, v

@@ -37,6 +37,11 @@
  *     groups=dim)), added to the attention output ([P1] §3 `out += lce(v)`).
  *     No residual and no output projection.
  *
+ *   - The Q/K/V projections of [P1] §3 (`q = self.q_proj(x)`, `k_proj`,
+ *     `v_proj`) are per-token linear maps with a bias (PyTorch nn.Linear's
+ *     default), given as one weight [3C][C] (rows 0..C-1 for q, C..2C-1 for
+ *     k, 2C..3C-1 for v) and one bias [3C].
+ *
  * All tensors are contiguous channels-last [B, H, W, C] arrays of double.
  * Functions return 0 on success and 1 on an invalid argument.
  */
@@ -387,4 +392,26 @@ int oracle_forward(const double *q, const double *k, const double *v, int B,
   if (rc) return rc;
   return oracle_attend(q, k, v, idx, B, H, W, C, heads, S, topk, w, bias, ks,
                        out, nthreads);
+}
+
+/*
+ * [P1] §3 "线性投影获取Q,K,V": q = x W_q^T + b_q, k = x W_k^T + b_k,
+ * v = x W_v^T + b_v for every token (the projections act on each token alone,
+ * so the region reshape before them changes nothing). x is [M][C] (M tokens),
+ * w is [3C][C] in the nn.Linear [out][in] layout, bias is [3C] or NULL (zero);
+ * q, k and v are [M][C].
+ */
+int oracle_qkv_project(const double *x, int M, int C, const double *w, const double *bias,
+                       double *q, double *k, double *v) {
+  if (!x || !w || !q || !k || !v || M < 0 || C <= 0) return ORACLE_EINVAL;
+  double *outs[3] = {q, k, v};
+  for (int m = 0; m < M; ++m)
+    for (int t = 0; t < 3; ++t)
+      for (int j = 0; j < C; ++j) {
+        const double *wr = w + ((size_t)t * C + j) * C;
+        double acc = bias ? bias[(size_t)t * C + j] : 0.0;
+        for (int c = 0; c < C; ++c) acc += x[(size_t)m * C + c] * wr[c];
+        outs[t][(size_t)m * C + j] = acc;
+      }
+  return ORACLE_OK;
 }

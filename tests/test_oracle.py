@@ -347,3 +347,34 @@ def test_oracle_rejects_bad_arguments():
         oracle.route(x, x, 3, 10)  # topk > S^2
     with pytest.raises(ValueError):
         oracle.lepe(x, np.ones((4, 2, 2)), None)  # even kernel
+
+
+# ---------------------------------------------------------------- projections
+def test_qkv_projection_equals_a_library_matmul():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 6, 4, 16))
+    w = rng.standard_normal((48, 16))
+    b = rng.standard_normal(48)
+    q, k, v = oracle.qkv_project(x, w, b)
+    full = np.einsum("bhwc,oc->bhwo", x, w) + b  # numpy's contraction, independently
+    np.testing.assert_allclose(q, full[..., :16], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(k, full[..., 16:32], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(v, full[..., 32:], rtol=0, atol=1e-12)
+
+
+def test_qkv_projection_special_cases():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 5, 8))
+    eye = np.eye(8)
+    # stacked multiples of the identity: q = x, k = 2x, v = -x exactly
+    q, k, v = oracle.qkv_project(x, np.concatenate([eye, 2 * eye, -eye]), None)
+    assert np.array_equal(q, x) and np.array_equal(k, 2 * x) and np.array_equal(v, -x)
+    # zero weight: every token gets the bias
+    b = rng.standard_normal(24)
+    q, k, v = oracle.qkv_project(x, np.zeros((24, 8)), b)
+    assert np.array_equal(q, np.broadcast_to(b[:8], x.shape))
+    assert np.array_equal(v, np.broadcast_to(b[16:], x.shape))
+    # a permutation weight moves channels
+    perm = np.eye(8)[::-1]
+    q, _, _ = oracle.qkv_project(x, np.concatenate([perm, eye, eye]), None)
+    assert np.array_equal(q, x[..., ::-1])
