@@ -126,6 +126,15 @@ def algorithmic_work(wl: bra_synth.Workload) -> dict:
     return {"route": route, "attend": attend, "forward": fwd}
 
 
+def projection_work(wl: bra_synth.Workload) -> dict:
+    """Algorithmic work of the Q/K/V projection of one batch: x read once, q,
+    k and v written once, the [3C, C] weight read once (bf16), and
+    2 M C 3C contraction flops."""
+    M, C = wl.B * wl.H * wl.W, wl.C
+    return {"bytes": 4 * M * C * 2 + 3 * C * C * 2, "tensor_flops": 6 * M * C * C,
+            "alu_flops": 0, "exps": 0}
+
+
 def peaks(sm_count: int | None = None, sm_mhz: float | None = None) -> dict:
     """Roofline denominators: HBM GB/s and bf16 tensor TFLOP/s measured on
     the B300s (MEASURED_PEAKS.json, burst figures for kernels timed
@@ -432,6 +441,45 @@ class Setup:
         self.torch.cuda.empty_cache()
 
 
+def time_projection(wl, dev, stream, steps: int) -> float:
+    """ms per bra_qkv_project launch over the workload's tokens, from CUDA
+    graphs over rotating input sets larger than L2."""
+    import torch
+    import vision_transformer_sparse_route_b300 as bra
+    M, C = wl.B * wl.H * wl.W, wl.C
+    x, w, b = bra_synth.make_projection_inputs(M, C, 0)
+    wd = torch.from_numpy(w).to(torch.bfloat16).to(dev)
+    bd = torch.from_numpy(b).to(dev)
+    per_set = 4 * M * C * 2
+    sets = max(2, -(-3 * L2_BYTES // per_set) + 1)
+    xh = torch.from_numpy(x).to(torch.bfloat16)
+    bufs = [(xh.to(dev), torch.empty((M, C), dtype=torch.bfloat16, device=dev),
+             torch.empty((M, C), dtype=torch.bfloat16, device=dev),
+             torch.empty((M, C), dtype=torch.bfloat16, device=dev)) for _ in range(sets)]
+    graphs = []
+    with torch.cuda.stream(stream):
+        for xs, q, k, v in bufs:
+            bra.qkv_project(xs, wd, bd, q, k, v, stream=stream)
+        stream.synchronize()
+        for xs, q, k, v in bufs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                bra.qkv_project(xs, wd, bd, q, k, v, stream=stream)
+            graphs.append(g)
+        for i in range(3):
+            graphs[i % sets].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % sets].replay()
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del graphs, bufs
+    torch.cuda.empty_cache()
+    return ms
+
+
 def launch_floor(torch, stream, reps: int = 2000) -> dict:
     """Replay cost of a CUDA graph holding one near-empty kernel (a
     one-element fill) and one holding two of them in a chain, back to back
@@ -479,6 +527,11 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
     if (wl.dtype == "bf16" and wl.C == 64 and wl.heads == 2 and wl.H // wl.S == 8
             and wl.W // wl.S == 8 and wl.topk <= 4 and wl.ks in (1, 3, 5)):
         tc_ms = st.time_kernel(st.attend_tc, kernel_steps)
+    # the Q/K/V projection that produces this workload's q, k, v (bf16, C a
+    # multiple of 64 up to 256)
+    proj_ms = None
+    if wl.dtype == "bf16" and wl.C % 64 == 0 and wl.C <= 256:
+        proj_ms = time_projection(wl, dev, stream, kernel_steps)
     work = algorithmic_work(wl)
     ok = st.bra.device_status(stream)
     launches = st.launches()
@@ -491,6 +544,10 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
              "step_roofline": roofline(work["forward"], pk, wl.dtype, ms * 1e-3),
              "route_roofline": roofline(work["route"], pk, wl.dtype, route_ms * 1e-3),
              "attend_roofline": roofline(work["attend"], pk, wl.dtype, attend_ms * 1e-3),
+             **({"qkv_project_us": proj_ms * 1e3,
+                 "qkv_project_roofline": roofline(projection_work(wl), pk, wl.dtype,
+                                                  proj_ms * 1e-3)}
+                if proj_ms is not None else {}),
              **({"attend_tc_us": tc_ms * 1e3,
                  "attend_tc_roofline": roofline(work["attend"], pk, wl.dtype, tc_ms * 1e-3)}
                 if tc_ms is not None else {}),

@@ -201,3 +201,16 @@ def normals_range(seed: int, first: int, count: int) -> np.ndarray:
     out[0::2] = r * np.cos(2.0 * np.pi * u2)
     out[1::2] = r * np.sin(2.0 * np.pi * u2)
     return out[:count]
+
+
+def make_projection_inputs(M: int, C: int, seed: int = 0):
+    """Seeded inputs of the Q/K/V projection: x [M, C] (N(0,1) per element),
+    w [3C, C] (N(0, 1/C), the scale of a default-initialised linear layer),
+    bias [3C] (0.02 N(0,1)); x and w rounded to bfloat16, all returned as
+    float32 holding the exact values both sides consume. Streams: seed * 256
+    + 8 (x), + 9 (w), + 10 (bias)."""
+    x = normals(seed * 256 + 8, M * C).reshape(M, C)
+    w = normals(seed * 256 + 9, 3 * C * C).reshape(3 * C, C) / np.sqrt(C)
+    b = 0.02 * normals(seed * 256 + 10, 3 * C)
+    return (round_bf16(x.astype(np.float32)), round_bf16(w.astype(np.float32)),
+            b.astype(np.float32))

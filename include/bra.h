@@ -165,6 +165,27 @@ int bra_forward_static(const void *q, const void *k, const void *v, int B,
                        int dtype, void *out, void *stream);
 
 /*
+ * bra_qkv_project -- the linear projections in front of BRA ("q =
+ * self.q_proj(x)", "k = self.k_proj(x)", "v = self.v_proj(x)" of the cybasar
+ * page §3), per token, on the tensor cores:
+ *   q[m][j] = sum_c x[m][c] w[j][c] + bias[j]
+ *   k[m][j] = sum_c x[m][c] w[C + j][c] + bias[C + j]
+ *   v[m][j] = sum_c x[m][c] w[2C + j][c] + bias[2C + j]
+ * with f32 accumulation and one rounding to bf16.
+ *   x        [M][C] device bf16 (e.g. a channels-last [B, H, W, C] map,
+ *            M = B H W)
+ *   w        [3C][C] device bf16, the [out][in] layout of a linear layer
+ *   bias     [3C] device float32, or NULL for none
+ *   q, k, v  out: [M][C] device bf16 each (the inputs of bra_forward)
+ * Supported: bf16, C a multiple of 64 from 64 to 256; otherwise
+ * BRA_ERR_UNSUPPORTED. Pointers 16-byte aligned, outputs disjoint from each
+ * other and from the inputs (else BRA_ERR_INVALID_ARG). M == 0 enqueues
+ * nothing.
+ */
+int bra_qkv_project(const void *x, const void *w, const float *bias, long long M, int C,
+                    int dtype, void *q, void *k, void *v, void *stream);
+
+/*
  * bra_forward_launches -- how many kernels bra_forward (and
  * bra_forward_static) enqueue for this problem on the current device: 1 or 2,
  * 0 for B == 0, or minus a status code for invalid sizes. Nothing is

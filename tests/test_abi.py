@@ -120,3 +120,18 @@ def test_wait_timeout_check_rejects_bad_limits(lib):
     assert lib.bra_check_wait_timeout(0, NULL) == bra.BRA_ERR_INVALID_ARG
     assert lib.bra_check_wait_timeout(999, NULL) == bra.BRA_ERR_INVALID_ARG
     assert lib.bra_check_wait_timeout(1_000_000_001, NULL) == bra.BRA_ERR_INVALID_ARG
+
+
+def test_projection_argument_errors(lib):
+    f = lib.bra_qkv_project
+    G = ctypes.c_void_p(0x70000000)
+    assert f(NULL, B_, NULL, 100, 64, 1, C_, D_, E_, NULL) == bra.BRA_ERR_INVALID_ARG
+    assert f(A, B_, NULL, -1, 64, 1, C_, D_, E_, NULL) == bra.BRA_ERR_INVALID_ARG
+    assert f(A, B_, NULL, 100, 64, 1, A, D_, E_, NULL) == bra.BRA_ERR_INVALID_ARG  # q aliases x
+    assert f(A, B_, NULL, 100, 64, 1, C_, C_, E_, NULL) == bra.BRA_ERR_INVALID_ARG  # q == k
+    assert f(A, B_, NULL, 100, 64, 1, ctypes.c_void_p(0x30000008), D_, E_, NULL) == \
+        bra.BRA_ERR_INVALID_ARG  # misaligned
+    assert f(A, B_, NULL, 100, 96, 1, C_, D_, E_, NULL) == bra.BRA_ERR_UNSUPPORTED
+    assert f(A, B_, NULL, 100, 512, 1, C_, D_, G, NULL) == bra.BRA_ERR_UNSUPPORTED
+    assert f(A, B_, NULL, 100, 64, 0, C_, D_, E_, NULL) == bra.BRA_ERR_UNSUPPORTED  # f32
+    assert f(NULL, NULL, NULL, 0, 64, 1, NULL, NULL, NULL, NULL) == bra.BRA_OK  # empty

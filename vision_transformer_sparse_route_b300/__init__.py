@@ -14,7 +14,7 @@ import os
 
 import torch
 
-__all__ = ["BraError", "route", "attend", "attend_tc", "forward", "forward_static", "forward_host",
+__all__ = ["BraError", "qkv_project", "route", "attend", "attend_tc", "forward", "forward_static", "forward_host",
            "HostPipeline",
            "idx_workspace_bytes", "forward_launches", "device_status", "check_wait_timeout", "library_path",
            "SYMBOLS"]
@@ -33,6 +33,7 @@ SYMBOLS = {
     "bra_attend_tc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "bra_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
     "bra_forward_static": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
+    "bra_qkv_project": (_I, [_P, _P, _P, ctypes.c_longlong, _I, _I, _P, _P, _P, _P]),
     "bra_idx_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "bra_forward_launches": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "bra_device_status": (_I, [_P, _I]),
@@ -142,6 +143,22 @@ def attend(q, k, v, idx, heads: int, S: int, lepe_w, lepe_b=None, out=None, stre
                             _dtype_code(q), _ptr(out), _stream(stream))
     _check(rc, "bra_attend")
     return out
+
+
+def qkv_project(x, w, bias=None, q=None, k=None, v=None, stream=None):
+    """(q, k, v) = the per-token projections x W^T + bias of a [..., C] bf16
+    tensor, with w [3C, C] bf16 and bias [3C] float32 (or None)."""
+    if not x.is_contiguous() or not w.is_contiguous():
+        raise ValueError("x and w must be contiguous")
+    C = x.shape[-1]
+    M = x.numel() // C
+    q = torch.empty_like(x) if q is None else q
+    k = torch.empty_like(x) if k is None else k
+    v = torch.empty_like(x) if v is None else v
+    rc = _load().bra_qkv_project(_ptr(x), _ptr(w), _ptr(bias), M, C, _dtype_code(x), _ptr(q),
+                                 _ptr(k), _ptr(v), _stream(stream))
+    _check(rc, "bra_qkv_project")
+    return q, k, v
 
 
 def attend_tc(q, k, v, idx, heads: int, S: int, lepe_w, lepe_b=None, out=None, stream=None):

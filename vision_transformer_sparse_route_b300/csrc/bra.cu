@@ -18,6 +18,7 @@
 #include "attend_f32.cuh"
 #include "attend_image.cuh"
 #include "attend_tc.cuh"
+#include "qkv_tc.cuh"
 #include "forward_image.cuh"
 #include "route.cuh"
 
@@ -99,6 +100,20 @@ bool make_map_t(CUtensorMap *m, const void *base, int dtype, int B, int H, int W
              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows][C] bf16 as a 2-D map; box = 64 channels x box_rows rows, 128-byte
+// swizzle, zero fill past the last row.
+bool make_map_2d(CUtensorMap *m, const void *base, int rows, int C, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap *m, const void *base, int B, int H, int W, int C,
@@ -470,6 +485,36 @@ bool plan_attend_tc(int B, int H, int W, int C, int heads, int S, int topk, int 
         return true;
       }
     }
+  return false;
+}
+
+// The projection kernel: C a multiple of 64 up to 256. W stays resident in
+// shared memory when it fits (C <= 128); ring depths are the deepest that fit.
+bool plan_qkv(int M, int C, bra::QkvGeom *g, size_t *smem) {
+  if (C % 64 || C < 64 || C > 256 || M <= 0) return false;
+  bra::QkvGeom a = {};
+  a.M = M; a.C = C;
+  a.ka = C / 64;
+  a.nt = 3 * C / 64;
+  a.tiles = (M + 127) / 128;
+  const size_t x_stage = (size_t)a.ka * 16384, w_stage = (size_t)a.ka * 8192;
+  const size_t tail = round_up((size_t)3 * C * 4, 16) + bra::kQbCount * 8 + 16;
+  struct Cfg { int nx, nw, ns, res; };
+  const Cfg cfgs[] = {{3, a.nt, 4, 1}, {2, a.nt, 4, 1}, {2, a.nt, 3, 1}, {2, 3, 2, 0},
+                      {2, 2, 2, 0}, {2, 2, 1, 0}, {1, 2, 1, 0}};
+  for (const Cfg &c : cfgs) {
+    if (c.res && a.nt > 12) continue;
+    a.nx = c.nx; a.nw = c.nw; a.ns = c.ns; a.w_resident = c.res;
+    a.off_w = (uint32_t)(c.nx * x_stage);
+    a.off_st = (uint32_t)(a.off_w + c.nw * w_stage);
+    a.off_b = a.off_st + (uint32_t)c.ns * 16384u;
+    a.off_bar = (uint32_t)round_up(a.off_b + (size_t)3 * C * 4, 16);
+    *smem = (size_t)a.off_st + (size_t)c.ns * 16384 + tail + 1024;
+    if (*smem <= kMaxSmemPerBlock) {
+      *g = a;
+      return true;
+    }
+  }
   return false;
 }
 
@@ -937,6 +982,41 @@ int bra_attend_tc(const void *q, const void *k, const void *v, const int32_t *id
     case 3: return launch_attend_tc_ks<3>(q, k, v, idx, B, C, lepe_w, lepe_b, out, g, smem, false, s);
     default: return launch_attend_tc_ks<5>(q, k, v, idx, B, C, lepe_w, lepe_b, out, g, smem, false, s);
   }
+}
+
+int bra_qkv_project(const void *x, const void *w, const float *bias, long long M, int C,
+                    int dtype, void *q, void *k, void *v, void *stream) {
+  if (M < 0 || C <= 0) return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_F32 && dtype != BRA_BF16) return BRA_ERR_INVALID_ARG;
+  if (M == 0) return BRA_OK;
+  if (!x || !w || !q || !k || !v) return BRA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return BRA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)M * C * 2;
+  const void *outs[3] = {q, k, v};
+  for (int i = 0; i < 3; ++i) {
+    if (overlap(outs[i], bytes, x, bytes) || overlap(outs[i], bytes, w, (size_t)3 * C * C * 2))
+      return BRA_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)
+      if (overlap(outs[i], bytes, outs[j], bytes)) return BRA_ERR_INVALID_ARG;
+  }
+  if (dtype != BRA_BF16 || M > 0x7fffffffll - 127) return BRA_ERR_UNSUPPORTED;
+  bra::QkvGeom g;
+  size_t smem;
+  if (!plan_qkv((int)M, C, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+  CUtensorMap tx, tw, tq, tk, tv;
+  if (!make_map_2d(&tx, x, (int)M, C, 128) || !make_map_2d(&tw, w, 3 * C, C, 64) ||
+      !make_map_2d(&tq, q, (int)M, C, 128) || !make_map_2d(&tk, k, (int)M, C, 128) ||
+      !make_map_2d(&tv, v, (int)M, C, 128))
+    return BRA_ERR_CUDA;
+  (void)cudaGetLastError();
+  auto kern = bra::bra_qkv_tc_kernel;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  const unsigned grid = (unsigned)std::min(g.tiles, sm_count());
+  kern<<<grid, bra::kQkvThreads, smem, static_cast<cudaStream_t>(stream)>>>(tx, tw, tq, tk, tv,
+                                                                           bias, g);
+  return cuda_status(cudaGetLastError());
 }
 
 int bra_forward_launches(int B, int H, int W, int C, int heads, int S, int topk, int lepe_ks,

@@ -1,0 +1,244 @@
+// qkv_tc.cuh -- the Q/K/V projections in front of BRA on the 5th-generation
+// tensor cores: q = x W_q^T + b_q, k = x W_k^T + b_k, v = x W_v^T + b_v for
+// every token (page "CVPR2023：BiFormer中的双层路由注意力机制解析" §3,
+// `q = self.q_proj(x)`, `k_proj`, `v_proj`), bf16 in, f32 accumulate, one
+// rounding to bf16.
+//
+// x is [M][C] (the tokens of a channels-last map), W [3C][C] in the [out][in]
+// layout of a linear layer (rows 0..C-1 give q, C..2C-1 k, 2C..3C-1 v), bias
+// [3C] f32. A persistent CTA per SM walks 128-token tiles of x:
+//   warp 0     TMA copies: the tile's x (C / 64 boxes of 128 tokens x 64
+//              channels, 128-byte swizzled) into a ring, and the weight tiles
+//              (64 output rows x 64 input channels): kept resident when the
+//              whole W fits (C <= 128), else streamed through a ring;
+//   warp 1     one thread issues, per 64-channel output tile n (3C / 64 of
+//              them), the C / 16 MMAs of D[128 x 64] = x_tile W_n^T (M = 128,
+//              N = 64, K = 16 each, both operands K-major) into one of four
+//              tensor-memory accumulators;
+//   warps 4-7  own the accumulators' 128 lanes (one token each): add the
+//              bias, round to bf16 into a 128-byte-swizzled staging tile and
+//              store it to q, k or v with one TMA copy.
+// Token tiles past M read zeros and their rows are not stored (TMA clips
+// them).
+#pragma once
+
+#include "attend_bf16.cuh"
+#include "tcgen05.cuh"
+
+namespace bra {
+
+constexpr int kQkvThreads = 256;
+constexpr uint32_t kQkvTmemCols = 256;  // four 64-column accumulators
+
+struct QkvGeom {
+  int M, C;
+  int ka;           // 64-channel atoms along K, C / 64
+  int nt;           // 64-channel output tiles, 3C / 64
+  int tiles;        // 128-token tiles
+  int nx, nw, ns;   // x ring (<= 4), weight ring (<= 12), staging ring (<= 4) depths
+  int w_resident;   // the whole W stays in shared memory (nw == nt)
+  uint32_t off_w, off_st, off_b, off_bar;  // x ring at 0
+};
+
+enum QkvBar {
+  kQbFx = 0,      // [4] x tile landed
+  kQbXfree = 4,   // [4] x tile read (MMA commit)
+  kQbFw = 8,      // [12] weight tile landed
+  kQbWfree = 20,  // [12] weight tile read (MMA commit)
+  kQbAfull = 32,  // [4] accumulator complete (MMA commit)
+  kQbAfree = 36,  // [4] accumulator read (128 arrivals)
+  kQbDone = 40,   // every MMA complete, before the tensor memory is freed
+  kQbCount = 41
+};
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void qkv_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(kQkvThreads, 1)
+    bra_qkv_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                      const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const float *__restrict__ bias, QkvGeom g) {
+  extern __shared__ uint8_t qkv_smem_raw[];
+  uint8_t *smem = qkv_smem_raw + ((1024u - (smem_u32(qkv_smem_raw) & 1023u)) & 1023u);
+  float *sb = reinterpret_cast<float *>(smem + g.off_b);  // [3C]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + g.off_bar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kQbCount);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int my_tiles = g.tiles > (int)blockIdx.x
+                           ? (g.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+                           : 0;
+  const uint32_t x_stage = (uint32_t)g.ka * 16384u, w_stage = (uint32_t)g.ka * 8192u;
+
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[kQbFx + i], 1);
+      mbar_init(&bars[kQbXfree + i], 1);
+    }
+    for (int i = 0; i < 12; ++i) {
+      mbar_init(&bars[kQbFw + i], 1);
+      mbar_init(&bars[kQbWfree + i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[kQbAfull + i], 1);
+      mbar_init(&bars[kQbAfree + i], 128);
+    }
+    mbar_init(&bars[kQbDone], 1);
+    fence_mbar_init();
+  }
+  for (int e = tid; e < 3 * g.C; e += kQkvThreads) sb[e] = bias ? __ldg(bias + e) : 0.f;
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kQkvTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ================================================= TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_x);
+      prefetch_tensormap(&tm_w);
+      int j = 0;  // weight tiles issued
+      for (int li = 0; li < my_tiles; ++li) {
+        const int tile = blockIdx.x + li * gridDim.x;
+        const int xs = li % g.nx;
+        mbar_wait(&bars[kQbXfree + xs], (uint32_t)(((li / g.nx) & 1) ^ 1));
+        mbar_arrive_expect_tx(&bars[kQbFx + xs], x_stage);
+        for (int a = 0; a < g.ka; ++a)
+          tma_load_2d(smem + xs * x_stage + a * 16384, &tm_x, &bars[kQbFx + xs], 64 * a,
+                      128 * tile);
+        if (g.w_resident && li > 0) continue;
+        for (int n = 0; n < g.nt; ++n, ++j) {
+          const int ws = j % g.nw;
+          if (!g.w_resident) mbar_wait(&bars[kQbWfree + ws], (uint32_t)(((j / g.nw) & 1) ^ 1));
+          mbar_arrive_expect_tx(&bars[kQbFw + ws], w_stage);
+          for (int a = 0; a < g.ka; ++a)
+            tma_load_2d(smem + g.off_w + ws * w_stage + a * 8192, &tm_w, &bars[kQbFw + ws],
+                        64 * a, 64 * n);
+        }
+      }
+      // no copy still in flight at exit
+      for (int li = (my_tiles > g.nx ? my_tiles - g.nx : 0); li < my_tiles; ++li)
+        mbar_drain(&bars[kQbFx + li % g.nx], (uint32_t)((li / g.nx) & 1));
+      for (int jj = (j > g.nw ? j - g.nw : 0); jj < j; ++jj)
+        mbar_drain(&bars[kQbFw + jj % g.nw], (uint32_t)((jj / g.nw) & 1));
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ====================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, 64, 0);
+      int j = 0, acc = 0;
+      for (int li = 0; li < my_tiles; ++li) {
+        const int xs = li % g.nx;
+        mbar_wait(&bars[kQbFx + xs], (uint32_t)((li / g.nx) & 1));
+        const uint32_t x0 = smem_u32(smem + xs * x_stage);
+        for (int n = 0; n < g.nt; ++n, ++acc) {
+          const int ws = g.w_resident ? n : j % g.nw;
+          mbar_wait(&bars[kQbFw + ws], g.w_resident ? 0u : (uint32_t)((j / g.nw) & 1));
+          const int as = acc & 3;
+          mbar_wait(&bars[kQbAfree + as], (uint32_t)(((acc >> 2) & 1) ^ 1));
+          tc_fence_after();
+          const uint32_t w0 = smem_u32(smem + g.off_w + ws * w_stage);
+          for (int a = 0; a < g.ka; ++a)
+            for (int s = 0; s < 4; ++s)
+              mma_bf16_ss(tmem + as * 64, smem_desc_sw128(x0 + a * 16384 + 32 * s, 1024),
+                          smem_desc_sw128(w0 + a * 8192 + 32 * s, 1024), idesc,
+                          (a > 0 || s > 0) ? 1u : 0u);
+          mma_commit(&bars[kQbAfull + as]);
+          if (!g.w_resident) {
+            mma_commit(&bars[kQbWfree + ws]);
+            ++j;
+          }
+        }
+        mma_commit(&bars[kQbXfree + xs]);
+      }
+      mma_commit(&bars[kQbDone]);
+      mbar_drain(&bars[kQbDone], 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ============================================ epilogue (TMEM lanes)
+    const int r = tid - 128;  // token row of the tile
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    int acc = 0;
+    for (int li = 0; li < my_tiles; ++li) {
+      const int tile = blockIdx.x + li * gridDim.x;
+      for (int n = 0; n < g.nt; ++n, ++acc) {
+        const int as = acc & 3, ss = acc % g.ns;
+        mbar_wait(&bars[kQbAfull + as], (uint32_t)((acc >> 2) & 1));
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld32(lane_base + as * 64, v0);
+        tmem_ld32(lane_base + as * 64 + 32, v1);
+        tmem_ld_wait();
+        tc_fence_before();
+        qkv_arrive(&bars[kQbAfree + as]);
+        // the store that last used this staging tile has read it
+        if (r == 0) {
+          if (g.ns == 1) tma_store_wait_read_n<0>();
+          else if (g.ns == 2) tma_store_wait_read_n<1>();
+          else if (g.ns == 3) tma_store_wait_read_n<2>();
+          else tma_store_wait_read_n<3>();
+        }
+        named_sync(1, 128);
+        uint8_t *row = smem + g.off_st + ss * 16384 + r * 128;
+        const float *bn = sb + n * 64;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: output channels 8c .. 8c+7
+          const uint32_t *src = c < 4 ? v0 + 8 * c : v1 + 8 * (c - 4);
+          const float4 b0 = *reinterpret_cast<const float4 *>(bn + 8 * c);
+          const float4 b1 = *reinterpret_cast<const float4 *>(bn + 8 * c + 4);
+          const uint4 packed = make_uint4(
+              pack_bf16x2(__uint_as_float(src[0]) + b0.x, __uint_as_float(src[1]) + b0.y),
+              pack_bf16x2(__uint_as_float(src[2]) + b0.z, __uint_as_float(src[3]) + b0.w),
+              pack_bf16x2(__uint_as_float(src[4]) + b1.x, __uint_as_float(src[5]) + b1.y),
+              pack_bf16x2(__uint_as_float(src[6]) + b1.z, __uint_as_float(src[7]) + b1.w));
+          *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = packed;
+        }
+        fence_async_shared();
+        named_sync(1, 128);
+        if (r == 0) {
+          const int t = n / g.ka, cc = n % g.ka;  // q, k or v; channel chunk
+          const CUtensorMap *map = t == 0 ? &tm_q : (t == 1 ? &tm_k : &tm_v);
+          tma_store_2d(map, smem + g.off_st + ss * 16384, 64 * cc, 128 * tile);
+          tma_store_commit();
+        }
+      }
+    }
+    if (r == 0) tma_store_wait_read();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kQkvTmemCols);
+  if (tid == 0) settle_after_timeout();
+}
+
+}  // namespace bra
