@@ -13,11 +13,13 @@
 //
 // One persistent CTA of 16 warps per SM walks the query regions ("units")
 // blockIdx.x, blockIdx.x + gridDim.x, ... . The warps have roles:
-//   warp 0     copies each unit's Q tile (TMA box) into a Q ring, one unit
-//              ahead, and turns the landed tile into a block-diagonal 128 x 64
-//              operand: rows 0-63 hold head 0's queries with channels 32-63
-//              zero, rows 64-127 head 1's with channels 0-31 zero, so that one
-//              M = 128 MMA computes both heads' logits against one K tile;
+//   warp 0     copies each unit's Q straight into a block-diagonal 128 x 64
+//              operand in a Q ring: two TMA boxes of one head's 32 channels
+//              (64-byte swizzled rows) land as [Q_h0][zeros][Q_h1], so that
+//              rows 0-63 hold head 0's queries with channels 32-63 zero and
+//              rows 64-127 head 1's with channels 0-31 zero (the two K atoms
+//              share the zero block), and one M = 128 MMA computes both
+//              heads' logits against one K tile;
 //   warp 1     one thread issues S = Q_bd K^T (M = 128, N = 64 topk, K = 64)
 //              into a tensor-memory slot and O = P V block by block (M = 128,
 //              N = 64, K = 64 keys per block) into the slot's first 64
@@ -29,9 +31,11 @@
 //   warps 4-7  own the 128 tensor-memory lanes (row r: head r / 64, query
 //              r % 64): the row maximum of S, P = 2^(S d^-1/2 log2 e - max) as
 //              bf16 (the operand of P V) into shared memory 64 keys at a time,
-//              the row sum of that bf16 P in f32; then, after the next unit's
-//              softmax, O / sum plus the LePE from the O tile, rounded once to
-//              bf16 into a staging tile that one thread stores with a TMA copy;
+//              the row sum of that bf16 P in f32 (or the MMA forms it); then
+//              O / sum plus the LePE from the O tile, rounded once to bf16
+//              into a staging tile that one thread stores with a TMA copy. Two
+//              such warpgroups take alternate units, so that one computes
+//              while the other waits for its P V;
 //   warps 8-15 the LePE stencil of each unit from the halo, ahead of the
 //              tensor cores, into an f32 O tile.
 // Only warp 3 reads the routing index, so when the kernel is launched right
@@ -54,11 +58,12 @@ constexpr uint32_t kTcTmemCols = 512;
 
 struct TcGeom {
   int H, W, S, topk, R, units;
-  int nh, nk, nv;           // halo, K and V ring stages (halo <= 4, K and V <= 2)
+  int nq, nh, nk, nv;       // Q, halo, K and V ring stages (Q <= 4, halo <= 4, K and V <= 2)
   int nslot;                // tensor-memory slots (<= 4)
   uint32_t slot_cols;       // columns of a slot (>= 64 topk, a power of two)
   int halo_w, halo_h;
   uint32_t off_h, off_k, off_v, off_ones, off_p, off_o, off_st, off_w, off_bar;  // Q ring at 0
+                            // (stages of 12 KB: Q_h0, zeros, Q_h1)
   int sum_mma;              // row sums from the P V MMA (one key block): N = 80, the
                             // 16 extra columns against a tile of ones
   uint32_t h_bytes;         // bytes of one halo stage
@@ -67,24 +72,23 @@ struct TcGeom {
 
 // Barrier slots (uint64 each) from off_bar; rings of up to four.
 enum TcBar {
-  kBarFq = 0,       // [2] Q tile landed (TMA)
-  kBarQready = 2,   // [2] block-diagonal Q built (1 arrival)
-  kBarQfree = 4,    // [2] Q operand read (MMA commit)
-  kBarFh = 6,       // [4] halo landed (TMA)
-  kBarHfree = 10,   // [4] halo read (256 LePE arrivals)
-  kBarFk = 14,      // [2] K tiles landed (TMA)
-  kBarKfree = 16,   // [2] K tiles read (MMA commit)
-  kBarFv = 18,      // [2] V tiles landed (TMA)
-  kBarVfree = 20,   // [2] V tiles read (MMA commit)
-  kBarSfull = 22,   // [4] S in a tensor-memory slot (MMA commit)
-  kBarOfull = 26,   // [4] O in a tensor-memory slot (MMA commit)
-  kBarTfree = 30,   // [4] slot read (128 arrivals)
-  kBarPfull = 34,   // [2] P block of softmax warpgroup g written (128 arrivals)
-  kBarPfree = 36,   // [2] P block of softmax warpgroup g read (MMA commit)
-  kBarOfill = 38,   // [2] LePE written into the O tile (256 arrivals)
-  kBarOfree = 40,   // [2] O tile consumed and stored (128 arrivals)
-  kBarDone = 42,    // every MMA complete (MMA commit), before the tensor memory is freed
-  kBarCount = 43
+  kBarFq = 0,       // [4] Q operand landed (TMA)
+  kBarQfree = 4,    // [4] Q operand read (MMA commit)
+  kBarFh = 8,       // [4] halo landed (TMA)
+  kBarHfree = 12,   // [4] halo read (256 LePE arrivals)
+  kBarFk = 16,      // [2] K tiles landed (TMA)
+  kBarKfree = 18,   // [2] K tiles read (MMA commit)
+  kBarFv = 20,      // [2] V tiles landed (TMA)
+  kBarVfree = 22,   // [2] V tiles read (MMA commit)
+  kBarSfull = 24,   // [4] S in a tensor-memory slot (MMA commit)
+  kBarOfull = 28,   // [4] O in a tensor-memory slot (MMA commit)
+  kBarTfree = 32,   // [4] slot read (128 arrivals)
+  kBarPfull = 36,   // [2] P block of softmax warpgroup g written (128 arrivals)
+  kBarPfree = 38,   // [2] P block of softmax warpgroup g read (MMA commit)
+  kBarOfill = 40,   // [2] LePE written into the O tile (256 arrivals)
+  kBarOfree = 42,   // [2] O tile consumed and stored (128 arrivals)
+  kBarDone = 44,    // every MMA complete (MMA commit), before the tensor memory is freed
+  kBarCount = 45
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
@@ -99,7 +103,7 @@ __device__ __forceinline__ uint32_t free_parity(int n) { return (uint32_t)((n & 
 
 template <int KS>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    bra_attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+    bra_attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,  // boxes of 32 channels
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_vh,
@@ -122,9 +126,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- set-up: barriers, weights, the permanent zeros of the Q operands
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kBarFq + i], 1);
-      mbar_init(&bars[kBarQready + i], 1);
-      mbar_init(&bars[kBarQfree + i], 1);
       mbar_init(&bars[kBarFk + i], 1);
       mbar_init(&bars[kBarKfree + i], 1);
       mbar_init(&bars[kBarFv + i], 1);
@@ -135,6 +136,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bars[kBarOfree + i], 128);
     }
     for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[kBarFq + i], 1);
+      mbar_init(&bars[kBarQfree + i], 1);
       mbar_init(&bars[kBarFh + i], 1);
       mbar_init(&bars[kBarHfree + i], kTcLepeThreads);
       mbar_init(&bars[kBarSfull + i], 1);
@@ -154,11 +157,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int e = tid; e < 8192 / 16; e += kTcThreads)
       *reinterpret_cast<uint4 *>(smem + g.off_ones + e * 16) =
           make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
-  // rows 64-127, chunks 0-3 of both Q operands stay zero
-  for (int e = tid; e < 2 * 64 * 4; e += kTcThreads) {
-    const int st = e >> 8, r = 64 + ((e >> 2) & 63), c = e & 3;
-    *reinterpret_cast<uint4 *>(smem + st * 16384 + swz128(r, c)) = make_uint4(0, 0, 0, 0);
-  }
+  // the zero block between Q_h0 and Q_h1 of every Q stage stays zero
+  for (int e = tid; e < g.nq * 256; e += kTcThreads)
+    *reinterpret_cast<uint4 *>(smem + (e >> 8) * 12288 + 4096 + (e & 255) * 16) =
+        make_uint4(0, 0, 0, 0);
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTcTmemCols);
     tmem_relinquish();
@@ -178,42 +180,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
 
   if (warp == 0) {
-    // ============================================= Q tiles and Q_bd builds
-    if (lane == 0) prefetch_tensormap(&tm_q);
-    auto issue_q = [&](int k) {
-      const int st = k & 1;
-      mbar_wait(&bars[kBarQfree + st], free_parity(k >> 1));
-      if (lane == 0) {
+    // ======================================================= Q producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      for (int k = 0; k < n_units; ++k) {
+        const int st = k % g.nq;
+        mbar_wait(&bars[kBarQfree + st], free_parity(k / g.nq));
         int b, y0, x0;
         unit_at(k, b, y0, x0);
         mbar_arrive_expect_tx(&bars[kBarFq + st], 8192);
-        tma_load_4d(smem + st * 16384, &tm_q, &bars[kBarFq + st], 0, x0, y0, b);
+        uint8_t *qs = smem + st * 12288;
+        tma_load_4d(qs, &tm_q, &bars[kBarFq + st], 0, x0, y0, b);          // head 0
+        tma_load_4d(qs + 8192, &tm_q, &bars[kBarFq + st], 32, x0, y0, b);  // head 1
       }
-      __syncwarp();
-    };
-    if (n_units > 0) issue_q(0);
-    for (int k = 0; k < n_units; ++k) {
-      if (k + 1 < n_units) issue_q(k + 1);
-      const int st = k & 1;
-      mbar_wait(&bars[kBarFq + st], full_parity(k >> 1));
-      // chunks 4-7 (head 1's channels) of rows 0-63 move to rows 64-127 (the
-      // same swizzled positions: a row and the row 64 below share r % 8)
-      uint8_t *a = smem + st * 16384;
-#pragma unroll
-      for (int e = lane; e < 256; e += 32) {
-        const int r = e >> 2, c = 4 + (e & 3);
-        uint4 *src = reinterpret_cast<uint4 *>(a + swz128(r, c));
-        *reinterpret_cast<uint4 *>(a + swz128(r + 64, c)) = *src;
-        *src = make_uint4(0, 0, 0, 0);
-      }
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarQready + st]);
+      // no Q copy still in flight at exit
+      for (int k = (n_units > g.nq ? n_units - g.nq : 0); k < n_units; ++k)
+        mbar_drain(&bars[kBarFq + k % g.nq], full_parity(k / g.nq));
     }
-    // no Q copy still in flight at exit (they were all waited for above,
-    // unless a wait gave up)
-    for (int k = (n_units > 2 ? n_units - 2 : 0); k < n_units; ++k)
-      mbar_drain(&bars[kBarFq + (k & 1)], full_parity(k >> 1));
+    __syncwarp();
   } else if (warp == 1) {
     // ====================================================== MMA issuer
     if (lane == 0) {
@@ -227,16 +211,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool progressed = false;
         // S of the next unit, as soon as its Q operand, K tiles and slot are ready
         if (next1 < n_units) {
-          const int k = next1, qs = k & 1, ks_ = k % g.nk, sl = k % g.nslot;
-          if (mbar_try_wait(&bars[kBarQready + qs], full_parity(k >> 1)) &&
+          const int k = next1, qs = k % g.nq, ks_ = k % g.nk, sl = k % g.nslot;
+          if (mbar_try_wait(&bars[kBarFq + qs], full_parity(k / g.nq)) &&
               mbar_try_wait(&bars[kBarFk + ks_], full_parity(k / g.nk)) &&
               mbar_try_wait(&bars[kBarTfree + sl], free_parity(k / g.nslot))) {
             tc_fence_after();
             const uint32_t d = tmem + sl * g.slot_cols;
-            const uint32_t a0 = smem_u32(smem + qs * 16384);
+            const uint32_t a0 = smem_u32(smem + qs * 12288);
             const uint32_t k0 = smem_u32(smem + g.off_k + ks_ * topk * 8192);
+            // K steps 0-1: channels 0-31 (rows 0-63 Q_h0, 64-127 zeros);
+            // K steps 2-3: channels 32-63 (rows 0-63 zeros, 64-127 Q_h1)
             for (int s = 0; s < 4; ++s)
-              mma_bf16_ss(d, smem_desc_sw128(a0 + 32 * s, 1024),
+              mma_bf16_ss(d, smem_desc_sw64(a0 + (s < 2 ? 32 * s : 4096 + 32 * (s - 2))),
                           smem_desc_sw128(k0 + 32 * s, 1024), idesc_s, s > 0);
             mma_commit(&bars[kBarSfull + sl]);
             mma_commit(&bars[kBarQfree + qs]);
@@ -354,7 +340,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float2 sc2 = make_float2(g.scale_log2, g.scale_log2);
     int pcnt = 0;  // P blocks this warpgroup has written (into its own buffer)
-    float inv_prev = 0.f;
     // O of unit k (in its slot, once out) / row sum, plus the LePE that the
     // LePE warps left in the O tile, rounded once to bf16 into the staging
     // tile, which one thread stores with a TMA copy
@@ -457,22 +442,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars[kBarPfull + wg]);
       }
-      const float inv = 1.f / ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-      if (g.nslot >= 4) {
-        // this warpgroup's previous unit (its O is out by now: its P V was
-        // issued before this unit's P was written); its slot is not the one
-        // the warpgroup's next unit needs
-        if (k >= 2) epilogue(k - 2, inv_prev);
-        inv_prev = inv;
-      } else {
-        // two slots: each warpgroup owns one, so its next unit's S can only
-        // be formed once this unit's O has been read
-        epilogue(k, inv);
-      }
-    }
-    if (g.nslot >= 4) {  // the last unit of this warpgroup
-      const int last = n_units - 1 - ((n_units - 1 - wg) & 1);
-      if (last >= wg) epilogue(last, inv_prev);
+      // this unit's O, as soon as its P V is out: while this warpgroup waits
+      // for it the other one computes its softmax
+      epilogue(k, 1.f / ((l4[0] + l4[1]) + (l4[2] + l4[3])));
     }
     if (r == 0) tma_store_wait_read();
   } else {

@@ -84,21 +84,25 @@ EncodeTiledFn encode_fn() {
 // box_h x 1 image, zero fill outside the map; 128-byte swizzle for tiles
 // read by ldmatrix.
 bool make_map_t(CUtensorMap *m, const void *base, int dtype, int B, int H, int W, int C,
-                int box_w, int box_h, bool swizzle) {
+                int box_w, int box_h, bool swizzle, int box_c = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t e = (cuuint64_t)elem_size(dtype);
   cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)C * e, (cuuint64_t)W * C * e,
                            (cuuint64_t)H * W * C * e};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / e), (cuuint32_t)box_w, (cuuint32_t)box_h, 1};
+  // box_c channels (default: 128 bytes of them); 64-byte rows take the
+  // 64-byte swizzle
+  const cuuint32_t bc = box_c ? (cuuint32_t)box_c : (cuuint32_t)(128 / e);
+  cuuint32_t box[4] = {bc, (cuuint32_t)box_w, (cuuint32_t)box_h, 1};
+  const CUtensorMapSwizzle sw = !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                : bc * e == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_128B;
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, dtype == BRA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
              4, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -466,11 +470,14 @@ bool plan_attend_tc(int B, int H, int W, int C, int heads, int S, int topk, int 
   const size_t w_bytes = (size_t)(ks * ks + 1) * 64 * 4;
   const size_t bars = (size_t)bra::kBarCount * 8 + 16;
   const size_t tile = (size_t)topk * 8192;  // K or V tiles of one unit
-  for (int nkv = 2; nkv >= 1; --nkv)
-    for (int nh = 3; nh >= 2; --nh) {
+  struct Depth { int nq, nh, nkv; };
+  const Depth depths[] = {{4, 3, 2}, {4, 2, 2}, {3, 2, 2}, {4, 2, 1}, {3, 2, 1}, {2, 2, 1}};
+  for (const Depth &dp : depths) {
+      const int nkv = dp.nkv, nh = dp.nh;
+      a.nq = dp.nq;
       a.nk = a.nv = nkv;
       a.nh = nh;
-      a.off_h = 2 * 16384;
+      a.off_h = (uint32_t)dp.nq * 12288u;
       a.off_k = (uint32_t)round_up((size_t)a.off_h + (size_t)nh * a.h_bytes, 1024);
       a.off_v = (uint32_t)(a.off_k + nkv * tile);
       a.off_ones = (uint32_t)(a.off_v + nkv * tile);
@@ -663,7 +670,7 @@ int launch_attend_tc_ks(const void *q, const void *k, const void *v, const int32
                         int C, const float *w, const float *bias, void *out, const TcGeom &g,
                         size_t smem, bool pdl, cudaStream_t s) {
   CUtensorMap tq, tk, tv, th, to;
-  if (!make_map(&tq, q, B, g.H, g.W, C, 8, 8, true) ||
+  if (!make_map_t(&tq, q, BRA_BF16, B, g.H, g.W, C, 8, 8, true, 32) ||
       !make_map(&tk, k, B, g.H, g.W, C, 8, 8, true) ||
       !make_map(&tv, v, B, g.H, g.W, C, 8, 8, true) ||
       !make_map(&th, v, B, g.H, g.W, C, g.halo_w, g.halo_h, false) ||
@@ -1006,8 +1013,8 @@ int bra_qkv_project(const void *x, const void *w, const float *bias, long long M
   if (!plan_qkv((int)M, C, &g, &smem)) return BRA_ERR_UNSUPPORTED;
   CUtensorMap tx, tw, tq, tk, tv;
   if (!make_map_2d(&tx, x, (int)M, C, 128) || !make_map_2d(&tw, w, 3 * C, C, 64) ||
-      !make_map_2d(&tq, q, (int)M, C, 128) || !make_map_2d(&tk, k, (int)M, C, 128) ||
-      !make_map_2d(&tv, v, (int)M, C, 128))
+      !make_map_2d(&tq, q, (int)M, C, 32) || !make_map_2d(&tk, k, (int)M, C, 32) ||
+      !make_map_2d(&tv, v, (int)M, C, 32))
     return BRA_ERR_CUDA;
   (void)cudaGetLastError();
   auto kern = bra::bra_qkv_tc_kernel;

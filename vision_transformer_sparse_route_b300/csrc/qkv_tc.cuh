@@ -16,8 +16,8 @@
 //              N = 64, K = 16 each, both operands K-major) into one of four
 //              tensor-memory accumulators;
 //   warps 4-7  own the accumulators' 128 lanes (one token each): add the
-//              bias, round to bf16 into a 128-byte-swizzled staging tile and
-//              store it to q, k or v with one TMA copy.
+//              bias, round to bf16 into a 128-byte-swizzled staging tile, and
+//              each warp stores its 32 rows to q, k or v with one TMA copy.
 // Token tiles past M read zeros and their rows are not stored (TMA clips
 // them).
 #pragma once
@@ -199,14 +199,14 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         qkv_arrive(&bars[kQbAfree + as]);
-        // the store that last used this staging tile has read it
-        if (r == 0) {
+        // this warp's store that last used this staging tile has read it
+        if (lane == 0) {
           if (g.ns == 1) tma_store_wait_read_n<0>();
           else if (g.ns == 2) tma_store_wait_read_n<1>();
           else if (g.ns == 3) tma_store_wait_read_n<2>();
           else tma_store_wait_read_n<3>();
         }
-        named_sync(1, 128);
+        __syncwarp();
         uint8_t *row = smem + g.off_st + ss * 16384 + r * 128;
         const float *bn = sb + n * 64;
 #pragma unroll
@@ -222,16 +222,18 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = packed;
         }
         fence_async_shared();
-        named_sync(1, 128);
-        if (r == 0) {
+        __syncwarp();
+        if (lane == 0) {  // each warp stores its own 32 rows
           const int t = n / g.ka, cc = n % g.ka;  // q, k or v; channel chunk
           const CUtensorMap *map = t == 0 ? &tm_q : (t == 1 ? &tm_k : &tm_v);
-          tma_store_2d(map, smem + g.off_st + ss * 16384, 64 * cc, 128 * tile);
+          const int w4 = warp & 3;
+          tma_store_2d(map, smem + g.off_st + ss * 16384 + w4 * 4096, 64 * cc,
+                       128 * tile + 32 * w4);
           tma_store_commit();
         }
       }
     }
-    if (r == 0) tma_store_wait_read();
+    if (lane == 0) tma_store_wait_read();
   }
 
   tc_fence_before();

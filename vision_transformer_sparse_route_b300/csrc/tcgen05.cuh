@@ -65,6 +65,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo)
   return d;
 }
 
+// Descriptor of a 64-byte-swizzled K-major tile: rows of 64 bytes (32 bf16),
+// the 16-byte chunk c of row r at chunk position c ^ ((r / 2) % 4), 8-row
+// groups 512 bytes apart, from a 512-byte aligned base; swizzle mode 4.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
+}
+
 // The same with a leading byte offset: for an MN-major tile wider than 64
 // elements along N, the distance from one 64-element atom to the next.
 __device__ __forceinline__ uint64_t smem_desc_sw128_lbo(uint32_t addr, uint32_t lbo,
