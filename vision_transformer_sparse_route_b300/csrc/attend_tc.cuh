@@ -11,7 +11,7 @@
 // Bi-Level-Routing-Attention": attention over the union of the routed
 // regions, with dense matrix products only).
 //
-// One persistent CTA of 16 warps per SM walks the query regions ("units")
+// One persistent CTA of 20 warps per SM walks the query regions ("units")
 // blockIdx.x, blockIdx.x + gridDim.x, ... . The warps have roles:
 //   warp 0     copies each unit's Q straight into a block-diagonal 128 x 64
 //              operand in a Q ring: two TMA boxes of one head's 32 channels
@@ -19,15 +19,17 @@
 //              rows 0-63 hold head 0's queries with channels 32-63 zero and
 //              rows 64-127 head 1's with channels 0-31 zero (the two K atoms
 //              share the zero block), and one M = 128 MMA computes both
-//              heads' logits against one K tile;
+//              heads' logits against one K tile; and each unit's V halo
+//              (region plus ks/2 border, zero filled outside the image) into
+//              a halo ring;
 //   warp 1     one thread issues S = Q_bd K^T (M = 128, N = 64 topk, K = 64)
 //              into a tensor-memory slot and O = P V block by block (M = 128,
 //              N = 64, K = 64 keys per block) into the slot's first 64
-//              columns, whichever has its inputs first;
-//   warp 2     copies each unit's V halo (region plus ks/2 border, zero filled
-//              outside the image) into a halo ring;
-//   warp 3     reads the routing and copies the routed regions' K and V tiles
-//              by index into a K ring and a V ring;
+//              columns, whichever has its inputs first (it polls without
+//              blocking);
+//   warps 2, 3 read the routing (one unit ahead) and copy the routed
+//              regions' K tiles (warp 2) and V tiles (warp 3) by index into a
+//              K ring and a V ring, each as soon as its own ring has room;
 //   warps 4-7  own the 128 tensor-memory lanes (row r: head r / 64, query
 //              r % 64): the row maximum of S, P = 2^(S d^-1/2 log2 e - max) as
 //              bf16 (the operand of P V) into shared memory 64 keys at a time,
@@ -36,9 +38,10 @@
 //              into a staging tile that one thread stores with a TMA copy. Two
 //              such warpgroups take alternate units, so that one computes
 //              while the other waits for its P V;
-//   warps 8-15 the LePE stencil of each unit from the halo, ahead of the
-//              tensor cores, into an f32 O tile.
-// Only warp 3 reads the routing index, so when the kernel is launched right
+//   warps 12-19 the LePE stencil of each unit from the halo, ahead of the
+//              tensor cores, into an f32 O tile (a thread: one channel pair,
+//              one column, eight rows).
+// Only warps 2 and 3 read the routing index, so when the kernel is launched right
 // after the routing grid (programmatic dependent launch) everything else --
 // Q tiles, halos, LePE -- starts before that grid has finished. Every ring,
 // slot and tile hand-off is an mbarrier, every wait bounded. The operand
@@ -58,7 +61,7 @@ constexpr uint32_t kTcTmemCols = 512;
 
 struct TcGeom {
   int H, W, S, topk, R, units;
-  int nq, nh, nk, nv;       // Q, halo, K and V ring stages (Q <= 4, halo <= 4, K and V <= 2)
+  int nq, nh, nk, nv;       // Q, halo, K and V ring stages (each <= 4)
   int nslot;                // tensor-memory slots (<= 4)
   uint32_t slot_cols;       // columns of a slot (>= 64 topk, a power of two)
   int halo_w, halo_h;
@@ -76,19 +79,19 @@ enum TcBar {
   kBarQfree = 4,    // [4] Q operand read (MMA commit)
   kBarFh = 8,       // [4] halo landed (TMA)
   kBarHfree = 12,   // [4] halo read (256 LePE arrivals)
-  kBarFk = 16,      // [2] K tiles landed (TMA)
-  kBarKfree = 18,   // [2] K tiles read (MMA commit)
-  kBarFv = 20,      // [2] V tiles landed (TMA)
-  kBarVfree = 22,   // [2] V tiles read (MMA commit)
-  kBarSfull = 24,   // [4] S in a tensor-memory slot (MMA commit)
-  kBarOfull = 28,   // [4] O in a tensor-memory slot (MMA commit)
-  kBarTfree = 32,   // [4] slot read (128 arrivals)
-  kBarPfull = 36,   // [2] P block of softmax warpgroup g written (128 arrivals)
-  kBarPfree = 38,   // [2] P block of softmax warpgroup g read (MMA commit)
-  kBarOfill = 40,   // [2] LePE written into the O tile (256 arrivals)
-  kBarOfree = 42,   // [2] O tile consumed and stored (128 arrivals)
-  kBarDone = 44,    // every MMA complete (MMA commit), before the tensor memory is freed
-  kBarCount = 45
+  kBarFk = 16,      // [4] K tiles landed (TMA)
+  kBarKfree = 20,   // [4] K tiles read (MMA commit)
+  kBarFv = 24,      // [4] V tiles landed (TMA)
+  kBarVfree = 28,   // [4] V tiles read (MMA commit)
+  kBarSfull = 32,   // [4] S in a tensor-memory slot (MMA commit)
+  kBarOfull = 36,   // [4] O in a tensor-memory slot (MMA commit)
+  kBarTfree = 40,   // [4] slot read (128 arrivals)
+  kBarPfull = 44,   // [2] P block of softmax warpgroup g written (128 arrivals)
+  kBarPfree = 46,   // [2] P block of softmax warpgroup g read (MMA commit)
+  kBarOfill = 48,   // [2] LePE written into the O tile (256 arrivals)
+  kBarOfree = 50,   // [2] O tile consumed and stored (128 arrivals)
+  kBarDone = 52,    // every MMA complete (MMA commit), before the tensor memory is freed
+  kBarCount = 53
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
@@ -126,10 +129,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- set-up: barriers, weights, the permanent zeros of the Q operands
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kBarFk + i], 1);
-      mbar_init(&bars[kBarKfree + i], 1);
-      mbar_init(&bars[kBarFv + i], 1);
-      mbar_init(&bars[kBarVfree + i], 1);
       mbar_init(&bars[kBarPfull + i], 128);
       mbar_init(&bars[kBarPfree + i], 1);
       mbar_init(&bars[kBarOfill + i], kTcLepeThreads);
@@ -140,6 +139,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bars[kBarQfree + i], 1);
       mbar_init(&bars[kBarFh + i], 1);
       mbar_init(&bars[kBarHfree + i], kTcLepeThreads);
+      mbar_init(&bars[kBarFk + i], 1);
+      mbar_init(&bars[kBarKfree + i], 1);
+      mbar_init(&bars[kBarFv + i], 1);
+      mbar_init(&bars[kBarVfree + i], 1);
       mbar_init(&bars[kBarSfull + i], 1);
       mbar_init(&bars[kBarOfull + i], 1);
       mbar_init(&bars[kBarTfree + i], 128);
@@ -180,22 +183,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
 
   if (warp == 0) {
-    // ======================================================= Q producer
+    // ============================================ Q and halo producer
     if (lane == 0) {
       prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_vh);
       for (int k = 0; k < n_units; ++k) {
-        const int st = k % g.nq;
-        mbar_wait(&bars[kBarQfree + st], free_parity(k / g.nq));
         int b, y0, x0;
         unit_at(k, b, y0, x0);
+        const int st = k % g.nq;
+        mbar_wait(&bars[kBarQfree + st], free_parity(k / g.nq));
         mbar_arrive_expect_tx(&bars[kBarFq + st], 8192);
         uint8_t *qs = smem + st * 12288;
         tma_load_4d(qs, &tm_q, &bars[kBarFq + st], 0, x0, y0, b);          // head 0
         tma_load_4d(qs + 8192, &tm_q, &bars[kBarFq + st], 32, x0, y0, b);  // head 1
+        const int hs = k % g.nh;
+        mbar_wait(&bars[kBarHfree + hs], free_parity(k / g.nh));
+        mbar_arrive_expect_tx(&bars[kBarFh + hs], g.h_bytes);
+        tma_load_4d(smem + g.off_h + hs * g.h_bytes, &tm_vh, &bars[kBarFh + hs], 0, x0 - PAD,
+                    y0 - PAD, b);
       }
-      // no Q copy still in flight at exit
+      // no Q or halo copy still in flight at exit
       for (int k = (n_units > g.nq ? n_units - g.nq : 0); k < n_units; ++k)
         mbar_drain(&bars[kBarFq + k % g.nq], full_parity(k / g.nq));
+      for (int k = (n_units > g.nh ? n_units - g.nh : 0); k < n_units; ++k)
+        mbar_drain(&bars[kBarFh + k % g.nh], full_parity(k / g.nh));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -205,16 +216,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t idesc_o = idesc_bf16_f32(128, g.sum_mma ? 80 : 64, 1);
       int next1 = 0;           // next unit for S = Q_bd K^T
       int next2 = 0, blk = 0;  // next unit and key block for O = P V
-      int pcnt[2] = {0, 0};    // P blocks consumed so far from each warpgroup's buffer
+      int pcnt0 = 0, pcnt1 = 0;  // P blocks consumed so far from each warpgroup's buffer
       uint64_t t_idle = 0;
+      unsigned n_idle = 0;
       while (next2 < n_units) {
         bool progressed = false;
         // S of the next unit, as soon as its Q operand, K tiles and slot are ready
         if (next1 < n_units) {
           const int k = next1, qs = k % g.nq, ks_ = k % g.nk, sl = k % g.nslot;
-          if (mbar_try_wait(&bars[kBarFq + qs], full_parity(k / g.nq)) &&
-              mbar_try_wait(&bars[kBarFk + ks_], full_parity(k / g.nk)) &&
-              mbar_try_wait(&bars[kBarTfree + sl], free_parity(k / g.nslot))) {
+          if (mbar_test_wait(&bars[kBarFq + qs], full_parity(k / g.nq)) &&
+              mbar_test_wait(&bars[kBarFk + ks_], full_parity(k / g.nk)) &&
+              mbar_test_wait(&bars[kBarTfree + sl], free_parity(k / g.nslot))) {
             tc_fence_after();
             const uint32_t d = tmem + sl * g.slot_cols;
             const uint32_t a0 = smem_u32(smem + qs * 12288);
@@ -234,8 +246,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the next P block of the oldest unit whose S is out, once written
         if (next2 < next1) {
           const int k = next2, pb = k & 1, vs = k % g.nv, sl = k % g.nslot;
-          if (mbar_try_wait(&bars[kBarPfull + pb], full_parity(pcnt[pb])) &&
-              (blk > 0 || mbar_try_wait(&bars[kBarFv + vs], full_parity(k / g.nv)))) {
+          if (mbar_test_wait(&bars[kBarPfull + pb], full_parity(pb ? pcnt1 : pcnt0)) &&
+              (blk > 0 || mbar_test_wait(&bars[kBarFv + vs], full_parity(k / g.nv)))) {
             tc_fence_after();
             const uint32_t d = tmem + sl * g.slot_cols;
             const uint32_t p0 = smem_u32(smem + g.off_p + pb * 16384);
@@ -246,7 +258,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           smem_desc_sw128_lbo(v0 + s * 2048, g.sum_mma ? lbo : 0u, 1024),
                           idesc_o, (blk > 0 || s > 0) ? 1u : 0u);
             mma_commit(&bars[kBarPfree + pb]);
-            ++pcnt[pb];
+            if (pb) ++pcnt1; else ++pcnt0;
             if (++blk == topk) {
               mma_commit(&bars[kBarOfull + sl]);
               mma_commit(&bars[kBarVfree + vs]);
@@ -256,81 +268,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             progressed = true;
           }
         }
-        // give up (and flag it) if nothing moves for as long as a bounded wait
+        // give up (and flag it) if nothing moves for as long as a bounded
+        // wait; the clock is read once every 1024 idle polls
         if (progressed) {
           t_idle = 0;
-        } else if (t_idle == 0) {
-          t_idle = global_ns();
-        } else if (global_ns() - t_idle > kWaitLimitNs ||
-                   (*reinterpret_cast<volatile unsigned *>(&g_status) & kStatusTimeout)) {
-          atomicOr(&g_status, kStatusTimeout);
-          break;
+          n_idle = 0;
+        } else if ((++n_idle & 1023) == 0) {
+          if (t_idle == 0) {
+            t_idle = global_ns();
+          } else if (global_ns() - t_idle > kWaitLimitNs ||
+                     (*reinterpret_cast<volatile unsigned *>(&g_status) & kStatusTimeout)) {
+            atomicOr(&g_status, kStatusTimeout);
+            break;
+          }
         }
       }
       mma_commit(&bars[kBarDone]);
       mbar_drain(&bars[kBarDone], 0);  // every MMA complete before the memory is freed
     }
     __syncwarp();
-  } else if (warp == 2) {
-    // ================================================= halo producer
-    if (lane == 0) {
-      prefetch_tensormap(&tm_vh);
-      for (int k = 0; k < n_units; ++k) {
-        const int st = k % g.nh;
-        mbar_wait(&bars[kBarHfree + st], free_parity(k / g.nh));
-        int b, y0, x0;
-        unit_at(k, b, y0, x0);
-        mbar_arrive_expect_tx(&bars[kBarFh + st], g.h_bytes);
-        tma_load_4d(smem + g.off_h + st * g.h_bytes, &tm_vh, &bars[kBarFh + st], 0, x0 - PAD,
-                    y0 - PAD, b);
-      }
-      // no halo copy still in flight at exit
-      for (int k = (n_units > g.nh ? n_units - g.nh : 0); k < n_units; ++k)
-        mbar_drain(&bars[kBarFh + k % g.nh], full_parity(k / g.nh));
-    }
-    __syncwarp();
-  } else if (warp == 3) {
-    // ================================================ K and V producer
-    if (lane == 0) {
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
-    }
+  } else if (warp == 2 || warp == 3) {
+    // ================================ K (warp 2) and V (warp 3) producers
+    const bool is_v = warp == 3;
+    const CUtensorMap *tm = is_v ? &tm_v : &tm_k;
+    const int nr = is_v ? g.nv : g.nk;
+    uint64_t *full = &bars[is_v ? kBarFv : kBarFk];
+    uint64_t *freed = &bars[is_v ? kBarVfree : kBarKfree];
+    uint8_t *ring = smem + (is_v ? g.off_v : g.off_k);
+    if (lane == 0) prefetch_tensormap(tm);
     grid_dependency_wait();  // the routing index comes from the previous grid
+    // lane m < topk copies routed region m; its index is read one unit ahead
+    int j_next = n_units > 0 && lane < topk ? __ldg(idx + (size_t)blockIdx.x * topk + lane) : 0;
     for (int k = 0; k < n_units; ++k) {
       const int u = blockIdx.x + k * gridDim.x;
-      const int b = u / g.R;
-      const int ks_ = k % g.nk, vs = k % g.nv;
-      const int j = lane < topk ? __ldg(idx + (size_t)u * topk + lane) : 0;
-      // lanes 0..topk-1: K of routed region lane; lanes 4..4+topk-1: its V
-      const int m = lane & 3;
-      const int jm = __shfl_sync(0xffffffffu, j, m);
-      const bool is_v = lane >= 4;
-      const bool active = lane < 8 && m < topk;
+      const int b = u / g.R, st = k % nr;
+      const int j = j_next;
+      if (k + 1 < n_units && lane < topk)
+        j_next = __ldg(idx + (size_t)(u + gridDim.x) * topk + lane);
       int xj = 0, yj = g.H;  // a box wholly below the image is all fill (zeros)
-      if (jm < 0 || jm >= g.R) {
-        if (active && !is_v) atomicOr(&g_status, kStatusBadIndex);
+      if (j < 0 || j >= g.R) {
+        if (lane < topk && !is_v) atomicOr(&g_status, kStatusBadIndex);
       } else {
-        xj = (jm % g.S) * 8;
-        yj = (jm / g.S) * 8;
+        xj = (j % g.S) * 8;
+        yj = (j / g.S) * 8;
       }
-      mbar_wait(&bars[kBarKfree + ks_], free_parity(k / g.nk));
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFk + ks_], topk * 8192);
+      mbar_wait(&freed[st], free_parity(k / nr));
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], topk * 8192);
       __syncwarp();
-      if (active && !is_v)
-        tma_load_4d(smem + g.off_k + (ks_ * topk + m) * 8192, &tm_k, &bars[kBarFk + ks_], 0, xj,
-                    yj, b);
-      mbar_wait(&bars[kBarVfree + vs], free_parity(k / g.nv));
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFv + vs], topk * 8192);
-      __syncwarp();
-      if (active && is_v)
-        tma_load_4d(smem + g.off_v + (vs * topk + m) * 8192, &tm_v, &bars[kBarFv + vs], 0, xj,
-                    yj, b);
+      if (lane < topk) tma_load_4d(ring + (st * topk + lane) * 8192, tm, &full[st], 0, xj, yj, b);
     }
     // no K or V copy still in flight at exit
-    for (int k = (n_units > g.nk ? n_units - g.nk : 0); k < n_units; ++k)
-      mbar_drain(&bars[kBarFk + k % g.nk], full_parity(k / g.nk));
-    for (int k = (n_units > g.nv ? n_units - g.nv : 0); k < n_units; ++k)
-      mbar_drain(&bars[kBarFv + k % g.nv], full_parity(k / g.nv));
+    for (int k = (n_units > nr ? n_units - nr : 0); k < n_units; ++k)
+      mbar_drain(&full[k % nr], full_parity(k / nr));
   } else if (warp < kTcLepeWarp0) {
     // ========================== softmax and O epilogue (TMEM lanes), two
     // warpgroups taking alternate units
@@ -398,9 +387,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       // the row maximum of the raw logits (four independent chains), 32
       // columns at a time
-      uint32_t v[32];
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       for (int c0 = 0; c0 < 64 * topk; c0 += 32) {
+        uint32_t v[32];
         tmem_ld32(srow + c0, v);
         tmem_ld_wait();
 #pragma unroll
@@ -416,27 +405,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // P (bf16) 64 keys at a time into this warpgroup's P buffer, and its
       // row sum (four chains) unless the MMA forms it
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint8_t *prow = smem + g.off_p + wg * 16384 + r * 128;
+      // 32 keys (16-byte chunks 4 half .. 4 half + 3) of P from the logits in v
+      auto emit = [&](const uint32_t(&v)[32], int half) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // 8 keys
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 8 * c + 2 * e;
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sc2, nb);
+            pk[e] = exp2_bf16x2(x.x, x.y);
+            if (!g.sum_mma) l4[e] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+          }
+          *reinterpret_cast<uint4 *>(prow + (((half * 4 + c) ^ (r & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      };
       for (int blk = 0; blk < topk; ++blk, ++pcnt) {
         mbar_wait(&bars[kBarPfree + wg], free_parity(pcnt));
-        uint8_t *prow = smem + g.off_p + wg * 16384 + r * 128;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
           tmem_ld32(srow + blk * 64 + half * 32, v);
           tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {  // 16-byte chunk half*4 + c: 8 keys
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 8 * c + 2 * e;
-              const float2 x = __ffma2_rn(
-                  make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sc2, nb);
-              pk[e] = exp2_bf16x2(x.x, x.y);
-              if (!g.sum_mma) l4[e] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
-            }
-            *reinterpret_cast<uint4 *>(prow + (((half * 4 + c) ^ (r & 7)) << 4)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
+          emit(v, half);
         }
         fence_async_shared();
         tc_fence_before();
@@ -448,7 +442,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (r == 0) tma_store_wait_read();
   } else {
-    // ======================================== LePE, O add, output store
+    // ================================================ LePE into the O tile
     const int lt = tid - 32 * kTcLepeWarp0;  // 0..255
     const int cp = lt & 31, x = lt >> 5;     // channel pair, column of the region
     const int c = 2 * cp;

@@ -471,7 +471,9 @@ bool plan_attend_tc(int B, int H, int W, int C, int heads, int S, int topk, int 
   const size_t bars = (size_t)bra::kBarCount * 8 + 16;
   const size_t tile = (size_t)topk * 8192;  // K or V tiles of one unit
   struct Depth { int nq, nh, nkv; };
-  const Depth depths[] = {{4, 3, 2}, {4, 2, 2}, {3, 2, 2}, {4, 2, 1}, {3, 2, 1}, {2, 2, 1}};
+  // Q and K rings equally deep (S needs both), the deepest that fit
+  const Depth depths[] = {{4, 2, 4}, {3, 2, 3}, {4, 3, 2}, {4, 2, 2}, {3, 2, 2},
+                          {2, 2, 2}, {3, 2, 1}, {2, 2, 1}};
   for (const Depth &dp : depths) {
       const int nkv = dp.nkv, nh = dp.nh;
       a.nq = dp.nq;

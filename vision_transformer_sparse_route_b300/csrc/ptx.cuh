@@ -64,6 +64,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of phase `parity` of `bar` (try_wait may suspend the
+// thread for a while; a thread that polls several barriers must not).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for phase `parity` of `bar` to complete, for at most limit_ns.
 // On giving up it sets kStatusTimeout and returns false; the caller carries
 // on (so that every thread still reaches every barrier of the block). Once
