@@ -86,13 +86,31 @@ def dist_env():
     return world, rank, local
 
 
-def sources_digest() -> str:
+def sources_digest(files=None) -> str:
+    """Digest of the given kernel sources (names under csrc/), by default of
+    every .cu/.cuh file there."""
+    names = files if files is not None else sorted(
+        n for n in os.listdir(CSRC) if n.endswith((".cu", ".cuh")))
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(names):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def kernel_sources(kernel: str, workload: str) -> list:
+    """The source files that define the device kernel `kernel` ("route" or
+    "attend") runs as for a workload: the kernel's own header and the headers
+    it includes. A recorded DRAM byte count stays valid while these are
+    unchanged."""
+    if kernel == "route":
+        return ["route.cuh", "ptx.cuh"]
+    wl = bra_synth.WORKLOADS[workload]
+    if wl.dtype == "f32":
+        return ["attend_f32.cuh", "ptx.cuh"]
+    if wl.H // wl.S * (wl.W // wl.S) < 16:  # regions under 16 tokens: image-resident kernel
+        return ["attend_image.cuh", "attend_bf16.cuh", "ptx.cuh"]
+    return ["attend_bf16.cuh", "ptx.cuh"]
 
 
 def algorithmic_bytes(wl: bra_synth.Workload) -> dict:
@@ -260,7 +278,7 @@ def recorded_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     e = rec.get(kernel, {}).get(workload)
-    if not e or e.get("sources") != sources_digest():
+    if not e or e.get("sources") != sources_digest(kernel_sources(kernel, workload)):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -18,8 +18,8 @@ def test_algorithmic_bytes_are_inputs_once_and_output_once():
 
 
 def test_recorded_traffic_only_for_matching_sources(tmp_path, monkeypatch):
-    rec = {"attend": {"stage1_bf16": {"sources": bench.sources_digest(),
-                                      "dram_bytes_per_launch": 123}},
+    src = bench.sources_digest(bench.kernel_sources("attend", "stage1_bf16"))
+    rec = {"attend": {"stage1_bf16": {"sources": src, "dram_bytes_per_launch": 123}},
            "route": {"stage1_bf16": {"sources": "0" * 16, "dram_bytes_per_launch": 456}}}
     path = tmp_path / "traffic.json"
     path.write_text(json.dumps(rec))
@@ -40,6 +40,24 @@ def test_sources_digest_covers_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.sources_digest() == d0
     (tmp_path / "b.cuh").write_text("z")
     assert bench.sources_digest() != d0
+    # a kernel's own digest ignores the other kernels' files
+    d1 = bench.sources_digest(["a.cu"])
+    (tmp_path / "b.cuh").write_text("zz")
+    assert bench.sources_digest(["a.cu"]) == d1
+    (tmp_path / "a.cu").write_text("xx")
+    assert bench.sources_digest(["a.cu"]) != d1
+
+
+def test_kernel_sources_follow_the_kernel_each_workload_runs():
+    assert bench.kernel_sources("route", "stage3_bf16") == ["route.cuh", "ptx.cuh"]
+    assert bench.kernel_sources("attend", "tiny_f32")[0] == "attend_f32.cuh"
+    assert bench.kernel_sources("attend", "stage3_bf16")[0] == "attend_image.cuh"
+    for name in ("stage1_bf16", "stage2_bf16", "seg512_bf16"):
+        assert bench.kernel_sources("attend", name)[0] == "attend_bf16.cuh"
+    for kernel in ("route", "attend"):
+        for name in bra_synth.WORKLOADS:
+            for f in bench.kernel_sources(kernel, name):
+                assert (bench.os.path.isfile(bench.os.path.join(bench.CSRC, f)))
 
 
 def test_measured_peak_falls_back_when_file_is_missing(tmp_path, monkeypatch):
