@@ -204,29 +204,27 @@ __device__ __forceinline__ void select_topk(const float (&val)[MAXJ], const floa
   }
 }
 
-// Grid (CL, B), cluster (CL, 1, 1), NT threads.
+// The routing of image b by one CTA of a cluster of CL CTAs (NT threads):
+// the CTA of rank r owns the regions r, r + CL, ... and writes their rows of
+// the routing index (and of the affinity, when given). route_smem is the
+// CTA's dynamic shared memory (layout of RouteGeom). On return no peer reads
+// this CTA's shared memory any more.
 // MAXJ = ceil(R / 32): affinity values each lane keeps for the top-k.
 // LOCAL_K: copy every K mean into local shared memory first (fast path);
 // otherwise read them from the peers' shared memory in the affinity loop.
-// At most 64 registers a thread (4 CTAs of 256 or one of 1024 per SM), except
-// for grids of more than 256 regions, whose rows keep more values a lane.
 template <typename T, int MAXJ, bool LOCAL_K, int NT, int SW>
-__global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
-    bra_route_kernel(const T *__restrict__ q, const T *__restrict__ k, RouteGeom g,
-                     int32_t *__restrict__ idx, float *__restrict__ affinity) {
-  // A dependent grid launched with programmatic serialization may start now;
-  // it waits for this grid before it reads the routing index.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+__device__ __forceinline__ void route_cta(const T *__restrict__ q, const T *__restrict__ k,
+                                          const RouteGeom &g, int32_t *__restrict__ idx,
+                                          float *__restrict__ affinity, uint8_t *route_smem,
+                                          int b) {
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  const int b = blockIdx.y;
   const int R = g.R, C = g.C;
   const int ro = (R - rank + CL - 1) / CL;  // owned regions rank, rank+CL, ...
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int VEC = Vec16<T>::N;
 
-  extern __shared__ __align__(16) uint8_t route_smem[];
   float *qm = reinterpret_cast<float *>(route_smem + g.off_qm);      // [ro_max][C]
   float *km = reinterpret_cast<float *>(route_smem + g.off_km);      // [ro_max][C]
   float *kall = reinterpret_cast<float *>(route_smem + g.off_kall);  // [R][C+1]
@@ -357,6 +355,20 @@ __global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
                       idx + ((size_t)b * R + i) * g.topk, nullptr);
   }
   if (!LOCAL_K) cluster.sync();  // keep km alive until every peer is done
+}
+
+// Grid (CL, B), cluster (CL, 1, 1), NT threads: route_cta for image blockIdx.y.
+// At most 64 registers a thread (4 CTAs of 256 or one of 1024 per SM), except
+// for grids of more than 256 regions, whose rows keep more values a lane.
+template <typename T, int MAXJ, bool LOCAL_K, int NT, int SW>
+__global__ void __launch_bounds__(NT, (MAXJ <= 8 ? 65536 / (64 * NT) : 1))
+    bra_route_kernel(const T *__restrict__ q, const T *__restrict__ k, RouteGeom g,
+                     int32_t *__restrict__ idx, float *__restrict__ affinity) {
+  // A dependent grid launched with programmatic serialization may start now;
+  // it waits for this grid before it reads the routing index.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  route_cta<T, MAXJ, LOCAL_K, NT, SW>(q, k, g, idx, affinity, route_smem, (int)blockIdx.y);
 }
 
 }  // namespace bra
