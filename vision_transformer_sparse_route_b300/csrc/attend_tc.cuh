@@ -94,16 +94,6 @@ enum TcBar {
   kBarCount = 53
 };
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Parity to wait for on a "full" barrier at the n-th use of its ring slot,
-// and on a "free" barrier (the first use of a slot does not wait: a fresh
-// barrier's preceding phase counts as complete).
-__device__ __forceinline__ uint32_t full_parity(int n) { return (uint32_t)(n & 1); }
-__device__ __forceinline__ uint32_t free_parity(int n) { return (uint32_t)((n & 1) ^ 1); }
-
 template <int KS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     bra_attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q,  // boxes of 32 channels

@@ -64,6 +64,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+// One arrival on bar (no transaction bytes).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Parity to wait for on a "full" barrier at the n-th use of its ring slot,
+// and on a "free" barrier (the first use of a slot does not wait: a fresh
+// barrier's preceding phase counts as complete).
+__device__ __forceinline__ uint32_t full_parity(int n) { return (uint32_t)(n & 1); }
+__device__ __forceinline__ uint32_t free_parity(int n) { return (uint32_t)((n & 1) ^ 1); }
+
 // Non-blocking test of phase `parity` of `bar` (try_wait may suspend the
 // thread for a while; a thread that polls several barriers must not).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
