@@ -509,11 +509,17 @@ bool plan_qkv(int M, int C, bra::QkvGeom *g, size_t *smem) {
   const size_t x_stage = (size_t)a.ka * 16384, w_stage = (size_t)a.ka * 8192;
   const size_t tail = round_up((size_t)3 * C * 4, 16) + bra::kQbCount * 8 + 16;
   struct Cfg { int nx, nw, ns, res; };
-  const Cfg cfgs[] = {{3, a.nt, 4, 1}, {2, a.nt, 4, 1}, {2, a.nt, 3, 1}, {2, 3, 2, 0},
-                      {2, 2, 2, 0}, {2, 2, 1, 0}, {1, 2, 1, 0}};
+  // staging tiles: one to three for each epilogue warpgroup
+  constexpr int E = bra::kQkvEpi;
+  const Cfg cfgs[] = {{4, a.nt, 3 * E, 1}, {3, a.nt, 3 * E, 1}, {2, a.nt, 3 * E, 1},
+                      {2, a.nt, 2 * E, 1}, {2, a.nt, E, 1},     {2, 3, 2 * E, 0},
+                      {2, 3, E, 0},        {2, 2, E, 0},        {1, 3, E, 0},
+                      {1, 2, E, 0}};
   for (const Cfg &c : cfgs) {
     if (c.res && a.nt > 12) continue;
     a.nx = c.nx; a.nw = c.nw; a.ns = c.ns; a.w_resident = c.res;
+    a.gw = c.res ? 3 : 1;
+    a.nacc = c.res ? 2 : 4;
     a.off_w = (uint32_t)(c.nx * x_stage);
     a.off_st = (uint32_t)(a.off_w + c.nw * w_stage);
     a.off_b = a.off_st + (uint32_t)c.ns * 16384u;
@@ -1013,18 +1019,17 @@ int bra_qkv_project(const void *x, const void *w, const float *bias, long long M
   bra::QkvGeom g;
   size_t smem;
   if (!plan_qkv((int)M, C, &g, &smem)) return BRA_ERR_UNSUPPORTED;
-  CUtensorMap tx, tw, tq, tk, tv;
-  if (!make_map_2d(&tx, x, (int)M, C, 128) || !make_map_2d(&tw, w, 3 * C, C, 64) ||
-      !make_map_2d(&tq, q, (int)M, C, 32) || !make_map_2d(&tk, k, (int)M, C, 32) ||
-      !make_map_2d(&tv, v, (int)M, C, 32))
+  CUtensorMap tx, tw;
+  if (!make_map_2d(&tx, x, (int)M, C, 128) || !make_map_2d(&tw, w, 3 * C, C, 64))
     return BRA_ERR_CUDA;
   (void)cudaGetLastError();
   auto kern = bra::bra_qkv_tc_kernel;
   if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
     return BRA_ERR_CUDA;
   const unsigned grid = (unsigned)std::min(g.tiles, sm_count());
-  kern<<<grid, bra::kQkvThreads, smem, static_cast<cudaStream_t>(stream)>>>(tx, tw, tq, tk, tv,
-                                                                           bias, g);
+  kern<<<grid, bra::kQkvThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      tx, tw, bias, g, static_cast<__nv_bfloat16 *>(q),
+      static_cast<__nv_bfloat16 *>(k), static_cast<__nv_bfloat16 *>(v));
   return cuda_status(cudaGetLastError());
 }
 

@@ -11,15 +11,23 @@
 //              channels, 128-byte swizzled) into a ring, and the weight tiles
 //              (64 output rows x 64 input channels): kept resident when the
 //              whole W fits (C <= 128), else streamed through a ring;
-//   warp 1     one thread issues, per 64-channel output tile n (3C / 64 of
-//              them), the C / 16 MMAs of D[128 x 64] = x_tile W_n^T (M = 128,
-//              N = 64, K = 16 each, both operands K-major) into one of four
-//              tensor-memory accumulators;
-//   warps 4-7  own the accumulators' 128 lanes (one token each): add the
-//              bias, round to bf16 into a 128-byte-swizzled staging tile, and
-//              each warp stores its 32 rows to q, k or v with one TMA copy.
-// Token tiles past M read zeros and their rows are not stored (TMA clips
-// them).
+//   warp 1     one thread issues, per group of output tiles (3 or 1
+//              64-channel tiles), the C / 16 MMAs of D = x_tile W_group^T
+//              (M = 128, N = 192 or 64, K = 16 each, both operands K-major)
+//              into one of the tensor-memory accumulators;
+//   warps 4-11, two epilogue warpgroups taking alternate accumulators,
+//              each owning the 128 lanes (one token each): add the bias,
+//              round to bf16 into a 128-byte-swizzled staging tile, and each
+//              warp copies its own 32 rows out to q, k or v with 16-byte
+//              stores, four whole rows (512 contiguous bytes) a warp
+//              instruction. (The SM's TMA unit takes about the same time for
+//              a box whatever its size; left to the x loads it keeps them
+//              short.)
+// With W resident (C <= 128) three 64-channel output tiles form one MMA
+// group of N = 192 against W stored atom-major ([ka][nt][64 rows], so the
+// group's 192 rows are contiguous): a third of the MMA instructions of
+// N = 64, whose issue rate is what bounds short bursts.
+// Token rows past M read zeros (the x copy's fill) and are not stored.
 #pragma once
 
 #include "attend_bf16.cuh"
@@ -27,16 +35,21 @@
 
 namespace bra {
 
-constexpr int kQkvThreads = 256;
-constexpr uint32_t kQkvTmemCols = 256;  // four 64-column accumulators
+constexpr int kQkvEpi = 2;                // epilogue warpgroups
+constexpr int kQkvThreads = 128 + 128 * kQkvEpi;
+constexpr uint32_t kQkvTmemCols = 512;
 
 struct QkvGeom {
   int M, C;
   int ka;           // 64-channel atoms along K, C / 64
   int nt;           // 64-channel output tiles, 3C / 64
   int tiles;        // 128-token tiles
-  int nx, nw, ns;   // x ring (<= 4), weight ring (<= 12), staging ring (<= 4) depths
-  int w_resident;   // the whole W stays in shared memory (nw == nt)
+  int nx, nw, ns;   // x ring (<= 4), weight ring (<= 12), staging tiles (1 to 3 for
+                    // each epilogue warpgroup)
+  int w_resident;   // the whole W stays in shared memory (nw == nt), stored atom-major
+                    // ([ka][nt][64 rows]) so that 3 output tiles form one N = 192 operand
+  int gw;           // output tiles per MMA group: 3 (N = 192) with W resident, else 1
+  int nacc;         // tensor-memory accumulators: 2 of 256 columns (gw 3) or 4 of 64
   uint32_t off_w, off_st, off_b, off_bar;  // x ring at 0
 };
 
@@ -45,10 +58,10 @@ enum QkvBar {
   kQbXfree = 4,   // [4] x tile read (MMA commit)
   kQbFw = 8,      // [12] weight tile landed
   kQbWfree = 20,  // [12] weight tile read (MMA commit)
-  kQbAfull = 32,  // [4] accumulator complete (MMA commit)
-  kQbAfree = 36,  // [4] accumulator read (128 arrivals)
-  kQbDone = 40,   // every MMA complete, before the tensor memory is freed
-  kQbCount = 41
+  kQbAfull = 32,  // [8] accumulator complete (MMA commit)
+  kQbAfree = 40,  // [8] accumulator read (128 arrivals)
+  kQbDone = 48,   // every MMA complete, before the tensor memory is freed
+  kQbCount = 49
 };
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
@@ -60,15 +73,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0,
-                                             int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1)
-      : "memory");
-}
-
 __device__ __forceinline__ void qkv_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -76,10 +80,9 @@ __device__ __forceinline__ void qkv_arrive(uint64_t *bar) {
 __global__ void __launch_bounds__(kQkvThreads, 1)
     bra_qkv_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_w,
-                      const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v,
-                      const float *__restrict__ bias, QkvGeom g) {
+                      const float *__restrict__ bias, QkvGeom g,
+                      __nv_bfloat16 *__restrict__ oq, __nv_bfloat16 *__restrict__ ok,
+                      __nv_bfloat16 *__restrict__ ov) {
   extern __shared__ uint8_t qkv_smem_raw[];
   uint8_t *smem = qkv_smem_raw + ((1024u - (smem_u32(qkv_smem_raw) & 1023u)) & 1023u);
   float *sb = reinterpret_cast<float *>(smem + g.off_b);  // [3C]
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       mbar_init(&bars[kQbFw + i], 1);
       mbar_init(&bars[kQbWfree + i], 1);
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 4; ++i) {  // up to four accumulators
       mbar_init(&bars[kQbAfull + i], 1);
       mbar_init(&bars[kQbAfree + i], 128);
     }
@@ -138,8 +141,10 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           if (!g.w_resident) mbar_wait(&bars[kQbWfree + ws], (uint32_t)(((j / g.nw) & 1) ^ 1));
           mbar_arrive_expect_tx(&bars[kQbFw + ws], w_stage);
           for (int a = 0; a < g.ka; ++a)
-            tma_load_2d(smem + g.off_w + ws * w_stage + a * 8192, &tm_w, &bars[kQbFw + ws],
-                        64 * a, 64 * n);
+            tma_load_2d(smem + g.off_w +
+                            (g.w_resident ? (uint32_t)(a * g.nt + n) * 8192u
+                                          : ws * w_stage + a * 8192u),
+                        &tm_w, &bars[kQbFw + ws], 64 * a, 64 * n);
         }
       }
       // no copy still in flight at exit
@@ -152,24 +157,30 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
   } else if (warp == 1) {
     // ====================================================== MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, 64, 0);
+      const uint32_t idesc = idesc_bf16_f32(128, 64 * g.gw, 0);
+      const uint32_t acc_cols = g.gw == 3 ? 256u : 64u;
       int j = 0, acc = 0;
       for (int li = 0; li < my_tiles; ++li) {
         const int xs = li % g.nx;
         mbar_wait(&bars[kQbFx + xs], (uint32_t)((li / g.nx) & 1));
         const uint32_t x0 = smem_u32(smem + xs * x_stage);
-        for (int n = 0; n < g.nt; ++n, ++acc) {
-          const int ws = g.w_resident ? n : j % g.nw;
-          mbar_wait(&bars[kQbFw + ws], g.w_resident ? 0u : (uint32_t)((j / g.nw) & 1));
-          const int as = acc & 3;
-          mbar_wait(&bars[kQbAfree + as], (uint32_t)(((acc >> 2) & 1) ^ 1));
+        // output tiles n0 .. n0 + gw - 1 as one MMA group (N = 64 gw)
+        for (int n0 = 0; n0 < g.nt; n0 += g.gw, ++acc) {
+          const int ws = g.w_resident ? n0 : j % g.nw;
+          for (int jj = 0; jj < g.gw; ++jj)
+            mbar_wait(&bars[kQbFw + ws + jj], g.w_resident ? 0u : (uint32_t)((j / g.nw) & 1));
+          const int as = acc % g.nacc;
+          mbar_wait(&bars[kQbAfree + as], free_parity(acc / g.nacc));
           tc_fence_after();
-          const uint32_t w0 = smem_u32(smem + g.off_w + ws * w_stage);
-          for (int a = 0; a < g.ka; ++a)
+          for (int a = 0; a < g.ka; ++a) {
+            const uint32_t w0 = smem_u32(
+                smem + g.off_w +
+                (g.w_resident ? (uint32_t)(a * g.nt + n0) * 8192u : ws * w_stage + a * 8192u));
             for (int s = 0; s < 4; ++s)
-              mma_bf16_ss(tmem + as * 64, smem_desc_sw128(x0 + a * 16384 + 32 * s, 1024),
-                          smem_desc_sw128(w0 + a * 8192 + 32 * s, 1024), idesc,
+              mma_bf16_ss(tmem + as * acc_cols, smem_desc_sw128(x0 + a * 16384 + 32 * s, 1024),
+                          smem_desc_sw128(w0 + 32 * s, 1024), idesc,
                           (a > 0 || s > 0) ? 1u : 0u);
+          }
           mma_commit(&bars[kQbAfull + as]);
           if (!g.w_resident) {
             mma_commit(&bars[kQbWfree + ws]);
@@ -184,28 +195,31 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ============================================ epilogue (TMEM lanes)
-    const int r = tid - 128;  // token row of the tile
+    const int eg = (warp - 4) >> 2;  // epilogue warpgroup: accumulators acc with acc % kQkvEpi == eg
+    const int r = (tid - 128) & 127;  // token row of the tile
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    int acc = 0;
+    const uint32_t acc_cols = g.gw == 3 ? 256u : 64u;
+    const int nsg = g.ns / kQkvEpi;  // staging tiles of this warpgroup
+    int acc = 0, cnt = 0;            // MMA groups seen; output tiles this warpgroup staged
     for (int li = 0; li < my_tiles; ++li) {
       const int tile = blockIdx.x + li * gridDim.x;
-      for (int n = 0; n < g.nt; ++n, ++acc) {
-        const int as = acc & 3, ss = acc % g.ns;
-        mbar_wait(&bars[kQbAfull + as], (uint32_t)((acc >> 2) & 1));
+      for (int n0 = 0; n0 < g.nt; n0 += g.gw, ++acc) {
+        if (acc % kQkvEpi != eg) continue;
+        const int as = acc % g.nacc;
+        mbar_wait(&bars[kQbAfull + as], full_parity(acc / g.nacc));
         tc_fence_after();
+        for (int jj = 0; jj < g.gw; ++jj, ++cnt) {
+        const int n = n0 + jj, ss = eg * nsg + cnt % nsg;
         uint32_t v0[32], v1[32];
-        tmem_ld32(lane_base + as * 64, v0);
-        tmem_ld32(lane_base + as * 64 + 32, v1);
+        tmem_ld32(lane_base + as * acc_cols + jj * 64, v0);
+        tmem_ld32(lane_base + as * acc_cols + jj * 64 + 32, v1);
         tmem_ld_wait();
-        tc_fence_before();
-        qkv_arrive(&bars[kQbAfree + as]);
-        // this warp's store that last used this staging tile has read it
-        if (lane == 0) {
-          if (g.ns == 1) tma_store_wait_read_n<0>();
-          else if (g.ns == 2) tma_store_wait_read_n<1>();
-          else if (g.ns == 3) tma_store_wait_read_n<2>();
-          else tma_store_wait_read_n<3>();
+        if (jj == g.gw - 1) {  // the accumulator is read
+          tc_fence_before();
+          qkv_arrive(&bars[kQbAfree + as]);
         }
+        // a warp stages and copies out only its own 32 rows: its previous
+        // copy from this staging tile is complete
         __syncwarp();
         uint8_t *row = smem + g.off_st + ss * 16384 + r * 128;
         const float *bn = sb + n * 64;
@@ -221,19 +235,27 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
               pack_bf16x2(__uint_as_float(src[6]) + b1.z, __uint_as_float(src[7]) + b1.w));
           *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = packed;
         }
-        fence_async_shared();
         __syncwarp();
-        if (lane == 0) {  // each warp stores its own 32 rows
+        // copy the staged rows out with the load/store units (the SM's TMA
+        // unit is left to the x loads): 4 whole rows, 512 contiguous bytes,
+        // per instruction
+        {
           const int t = n / g.ka, cc = n % g.ka;  // q, k or v; channel chunk
-          const CUtensorMap *map = t == 0 ? &tm_q : (t == 1 ? &tm_k : &tm_v);
-          const int w4 = warp & 3;
-          tma_store_2d(map, smem + g.off_st + ss * 16384 + w4 * 4096, 64 * cc,
-                       128 * tile + 32 * w4);
-          tma_store_commit();
+          __nv_bfloat16 *dst = t == 0 ? oq : (t == 1 ? ok : ov);
+          const uint8_t *tile_st = smem + g.off_st + ss * 16384;
+          const int w4 = warp & 3, ch = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 32 * w4 + 4 * i + (lane >> 3);
+            const long long m = 128ll * tile + rr;
+            const uint4 val =
+                *reinterpret_cast<const uint4 *>(tile_st + rr * 128 + ((ch ^ (rr & 7)) << 4));
+            if (m < g.M) *reinterpret_cast<uint4 *>(dst + m * g.C + 64 * cc + 8 * ch) = val;
+          }
+        }
         }
       }
     }
-    if (lane == 0) tma_store_wait_read();
   }
 
   tc_fence_before();
