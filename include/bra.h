@@ -111,8 +111,9 @@ int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
  * as bra_attend; other shapes return BRA_ERR_UNSUPPORTED. The result equals
  * bra_attend's within the bf16 tolerance (the exponentials and row sums are
  * formed in the same precision; the order of additions differs). On the
- * B300 this variant is measured slower than bra_attend for the stage-1 and
- * 512 x 512 shapes, so bra_forward does not use it.
+ * B300 this variant is measured as fast as bra_attend on the stage-1 shape
+ * alone but slower inside the forward and on the 512 x 512 shape, so
+ * bra_forward does not use it.
  */
 int bra_attend_tc(const void *q, const void *k, const void *v, const int32_t *idx, int B,
                   int H, int W, int C, int heads, int S, int topk, const float *lepe_w,

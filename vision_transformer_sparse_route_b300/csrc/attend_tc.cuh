@@ -35,12 +35,14 @@
 //              bf16 (the operand of P V) into shared memory 64 keys at a time,
 //              the row sum of that bf16 P in f32 (or the MMA forms it); then
 //              O / sum plus the LePE from the O tile, rounded once to bf16
-//              into a staging tile that one thread stores with a TMA copy. Two
+//              into a staging tile that the warpgroup copies out with
+//              coalesced 16-byte stores. Two
 //              such warpgroups take alternate units, so that one computes
 //              while the other waits for its P V;
 //   warps 12-19 the LePE stencil of each unit from the halo, ahead of the
-//              tensor cores, into an f32 O tile (a thread: one channel pair,
-//              one column, eight rows).
+//              tensor cores, into an f32 O tile: two groups of four warps on
+//              alternate units (a thread: one channel pair, two columns,
+//              eight rows).
 // Only warps 2 and 3 read the routing index, so when the kernel is launched right
 // after the routing grid (programmatic dependent launch) everything else --
 // Q tiles, halos, LePE -- starts before that grid has finished. Every ring,
@@ -55,7 +57,7 @@ namespace bra {
 
 constexpr int kTcWarps = 20;
 constexpr int kTcThreads = 32 * kTcWarps;
-constexpr int kTcLepeThreads = 256;   // warps 12-19
+constexpr int kTcLepeThreads = 256;   // warps 12-19, two groups of 128 on alternate units
 constexpr int kTcLepeWarp0 = 12;
 constexpr uint32_t kTcTmemCols = 512;
 
@@ -78,7 +80,7 @@ enum TcBar {
   kBarFq = 0,       // [4] Q operand landed (TMA)
   kBarQfree = 4,    // [4] Q operand read (MMA commit)
   kBarFh = 8,       // [4] halo landed (TMA)
-  kBarHfree = 12,   // [4] halo read (256 LePE arrivals)
+  kBarHfree = 12,   // [4] halo read (128 LePE arrivals)
   kBarFk = 16,      // [4] K tiles landed (TMA)
   kBarKfree = 20,   // [4] K tiles read (MMA commit)
   kBarFv = 24,      // [4] V tiles landed (TMA)
@@ -88,7 +90,7 @@ enum TcBar {
   kBarTfree = 40,   // [4] slot read (128 arrivals)
   kBarPfull = 44,   // [2] P block of softmax warpgroup g written (128 arrivals)
   kBarPfree = 46,   // [2] P block of softmax warpgroup g read (MMA commit)
-  kBarOfill = 48,   // [2] LePE written into the O tile (256 arrivals)
+  kBarOfill = 48,   // [2] LePE written into the O tile (128 arrivals)
   kBarOfree = 50,   // [2] O tile consumed and stored (128 arrivals)
   kBarDone = 52,    // every MMA complete (MMA commit), before the tensor memory is freed
   kBarCount = 53
@@ -100,9 +102,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_vh,
-                         const __grid_constant__ CUtensorMap tm_o,
                          const int32_t *__restrict__ idx, const float *__restrict__ lepe_w,
-                         const float *__restrict__ lepe_b, TcGeom g) {
+                         const float *__restrict__ lepe_b, TcGeom g,
+                         __nv_bfloat16 *__restrict__ out) {
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t *smem = tc_smem_raw + ((1024u - (smem_u32(tc_smem_raw) & 1023u)) & 1023u);
   float *sw = reinterpret_cast<float *>(smem + g.off_w);  // [KS*KS][64], bias [64]
@@ -121,14 +123,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kBarPfull + i], 128);
       mbar_init(&bars[kBarPfree + i], 1);
-      mbar_init(&bars[kBarOfill + i], kTcLepeThreads);
+      mbar_init(&bars[kBarOfill + i], kTcLepeThreads / 2);
       mbar_init(&bars[kBarOfree + i], 128);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars[kBarFq + i], 1);
       mbar_init(&bars[kBarQfree + i], 1);
       mbar_init(&bars[kBarFh + i], 1);
-      mbar_init(&bars[kBarHfree + i], kTcLepeThreads);
+      mbar_init(&bars[kBarHfree + i], kTcLepeThreads / 2);
       mbar_init(&bars[kBarFk + i], 1);
       mbar_init(&bars[kBarKfree + i], 1);
       mbar_init(&bars[kBarFv + i], 1);
@@ -334,8 +336,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars[kBarTfree + sl]);
       mbar_wait(&bars[kBarOfill + ot], full_parity(k >> 1));
-      // this warpgroup's previous store (from the same staging tile) has been read
-      if (r == 0) tma_store_wait_read();
+      // this warpgroup is done copying its previous unit out of the staging tile
       named_sync(3 + wg, 128);
       // O tile [64 tokens][16 chunks of 4 floats]: chunk c of token t sits at
       // chunk position c ^ (t % 8); staging tile [64 tokens][8 chunks of 8
@@ -360,13 +361,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         fmaf(__uint_as_float(v[8 * c + 7]), inv, l1.w)));
         *reinterpret_cast<uint4 *>(srow_st + (((h * 4 + c) ^ (tq & 7)) << 4)) = packed;
       }
-      fence_async_shared();
       named_sync(3 + wg, 128);
-      if (r == 0) {
+      // copy the staged unit out with the load/store units: 8 threads a
+      // token (its 128 bytes), four whole tokens a warp instruction (a TMA
+      // store would hold up its issuing thread, and with it this warpgroup's
+      // next P, for about half a microsecond)
+      {
         int b, y0, x0;
         unit_at(k, b, y0, x0);
-        tma_store_4d(&tm_o, smem + g.off_st + ot * 8192, 0, x0, y0, b);
-        tma_store_commit();
+        const uint8_t *st = smem + g.off_st + ot * 8192;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int e = it * 128 + r, t = e >> 3, ch = e & 7;
+          const uint4 val = *reinterpret_cast<const uint4 *>(st + t * 128 + ((ch ^ (t & 7)) << 4));
+          *reinterpret_cast<uint4 *>(
+              out + (((size_t)b * g.H + y0 + (t >> 3)) * g.W + x0 + (t & 7)) * 64 + 8 * ch) = val;
+        }
       }
       mbar_arrive(&bars[kBarOfree + ot]);
     };
@@ -430,36 +440,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // for it the other one computes its softmax
       epilogue(k, 1.f / ((l4[0] + l4[1]) + (l4[2] + l4[3])));
     }
-    if (r == 0) tma_store_wait_read();
   } else {
     // ================================================ LePE into the O tile
-    const int lt = tid - 32 * kTcLepeWarp0;  // 0..255
-    const int cp = lt & 31, x = lt >> 5;     // channel pair, column of the region
+    // two groups of four warps take alternate units; a thread: channel pair
+    // cp, region columns 2 xp and 2 xp + 1, all 8 rows (each halo value it
+    // loads feeds both columns)
+    const int lg = (warp - kTcLepeWarp0) >> 2;           // LePE group: units k % 2 == lg
+    const int lt = (tid - 32 * kTcLepeWarp0) & 127;      // 0..127
+    const int cp = lt & 31, xp = lt >> 5;
     const int c = 2 * cp;
     float2 wgt[KS * KS];
 #pragma unroll
     for (int e = 0; e < KS * KS; ++e) wgt[e] = *reinterpret_cast<const float2 *>(sw + e * 64 + c);
     const float2 bias = *reinterpret_cast<const float2 *>(sw + KS * KS * 64 + c);
-    for (int k = 0; k < n_units; ++k) {
+    for (int k = lg; k < n_units; k += 2) {
       const int hs = k % g.nh, ot = k & 1;
       mbar_wait(&bars[kBarFh + hs], full_parity(k / g.nh));
       const uint8_t *hb = smem + g.off_h + hs * g.h_bytes;
-      float2 acc[8];
+      float2 acc[2][8];
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) acc[rr] = bias;
-      const uint8_t *col = hb + x * 128 + c * 2;
+      for (int dx = 0; dx < 2; ++dx)
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) acc[dx][rr] = bias;
+      // halo rows yy, halo columns 2 xp .. 2 xp + KS: each value feeds both
+      // output columns (taps w and w - 1) and up to KS output rows
+      const uint8_t *col = hb + 2 * xp * 128 + c * 2;
 #pragma unroll
       for (int yy = 0; yy < 8 + KS - 1; ++yy) {
         const uint8_t *rp = col + yy * (8 + KS - 1) * 128;
 #pragma unroll
-        for (int w = 0; w < KS; ++w) {
+        for (int w = 0; w < KS + 1; ++w) {
           const uint32_t t2 = *reinterpret_cast<const uint32_t *>(rp + w * 128);
-          const float2 vv = make_float2(__uint_as_float(__byte_perm(t2, 0u, 0x1044u)),
-                                        __uint_as_float(__byte_perm(t2, 0u, 0x3244u)));
+          const float2 vv = make_float2(__uint_as_float(t2 << 16),
+                                        __uint_as_float(t2 & 0xffff0000u));
 #pragma unroll
-          for (int uu = 0; uu < KS; ++uu) {
-            const int rr = yy - uu;
-            if (rr >= 0 && rr < 8) acc[rr] = __ffma2_rn(wgt[uu * KS + w], vv, acc[rr]);
+          for (int dx = 0; dx < 2; ++dx) {
+            const int tw = w - dx;  // tap column for output column 2 xp + dx
+            if (tw < 0 || tw >= KS) continue;
+#pragma unroll
+            for (int uu = 0; uu < KS; ++uu) {
+              const int rr = yy - uu;
+              if (rr >= 0 && rr < 8) acc[dx][rr] = __ffma2_rn(wgt[uu * KS + tw], vv, acc[dx][rr]);
+            }
           }
         }
       }
@@ -468,11 +490,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait(&bars[kBarOfree + ot], free_parity(k >> 1));
       float *otile = reinterpret_cast<float *>(smem + g.off_o + ot * 16384);
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int t = rr * 8 + x;
-        *reinterpret_cast<float2 *>(otile + t * 64 + (((c >> 2) ^ (t & 7)) << 2) + (c & 3)) =
-            acc[rr];
-      }
+      for (int dx = 0; dx < 2; ++dx)
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const int t = rr * 8 + 2 * xp + dx;
+          *reinterpret_cast<float2 *>(otile + t * 64 + (((c >> 2) ^ (t & 7)) << 2) + (c & 3)) =
+              acc[dx][rr];
+        }
       mbar_arrive(&bars[kBarOfill + ot]);
     }
   }

@@ -677,12 +677,11 @@ template <int KS>
 int launch_attend_tc_ks(const void *q, const void *k, const void *v, const int32_t *idx, int B,
                         int C, const float *w, const float *bias, void *out, const TcGeom &g,
                         size_t smem, bool pdl, cudaStream_t s) {
-  CUtensorMap tq, tk, tv, th, to;
+  CUtensorMap tq, tk, tv, th;
   if (!make_map_t(&tq, q, BRA_BF16, B, g.H, g.W, C, 8, 8, true, 32) ||
       !make_map(&tk, k, B, g.H, g.W, C, 8, 8, true) ||
       !make_map(&tv, v, B, g.H, g.W, C, 8, 8, true) ||
-      !make_map(&th, v, B, g.H, g.W, C, g.halo_w, g.halo_h, false) ||
-      !make_map(&to, out, B, g.H, g.W, C, 8, 8, true))
+      !make_map(&th, v, B, g.H, g.W, C, g.halo_w, g.halo_h, false))
     return BRA_ERR_CUDA;
   auto kern = bra::bra_attend_tc_kernel<KS>;
   if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
@@ -697,7 +696,8 @@ int launch_attend_tc_ks(const void *q, const void *k, const void *v, const int32
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, th, to, idx, w, bias, g));
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, th, idx, w, bias, g,
+                                        static_cast<__nv_bfloat16 *>(out)));
 }
 
 template <int KS, int RB>
