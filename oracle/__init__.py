@@ -48,6 +48,7 @@ def _load():
             "oracle_attend": [P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, I],
             "oracle_forward": [P, P, P, I, I, I, I, I, I, I, P, P, I, P, P, I],
             "oracle_qkv_project": [P, I, I, P, P, P, P, P],
+            "oracle_layer_norm": [P, I, I, P, P, ctypes.c_double, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -183,3 +184,28 @@ def qkv_project(x, w, bias=None):
     _check(_load().oracle_qkv_project(_p(x), M, C, _p(w), _p(bias), _p(q), _p(k), _p(v)),
            "qkv_project")
     return q, k, v
+
+
+def layer_norm(x, gamma=None, beta=None, eps: float = 1e-5) -> np.ndarray:
+    """nn.LayerNorm over the last axis (biased variance), float64."""
+    x = _f64(x)
+    C = x.shape[-1]
+    gamma = None if gamma is None else _f64(gamma)
+    beta = None if beta is None else _f64(beta)
+    y = np.empty_like(x)
+    _check(_load().oracle_layer_norm(_p(x), int(np.prod(x.shape[:-1])), C, _p(gamma), _p(beta),
+                                     float(eps), _p(y)), "layer_norm")
+    return y
+
+
+def block_attention(x, ln_w, ln_b, w_qkv, b_qkv, heads: int, S: int, topk: int, lepe_w,
+                    lepe_b, eps: float = 1e-5, threads: int = 1):
+    """The attention branch of the BiFormer block (p3 "BiFormer架构核心思想解析"
+    §3.1): y = x + bra(norm1(x)), bra being the projections of p1 §3 followed
+    by the routed attention + LePE. Returns (y, idx, the stages: normalised x,
+    q, k, v)."""
+    x = _f64(x)
+    xn = layer_norm(x, ln_w, ln_b, eps)
+    q, k, v = qkv_project(xn, w_qkv, b_qkv)
+    out, idx = forward(q, k, v, heads, S, topk, lepe_w, lepe_b, threads=threads)
+    return x + out, idx, (xn, q, k, v)

@@ -41,6 +41,10 @@
  *     `v_proj`) are per-token linear maps with a bias (PyTorch nn.Linear's
  *     default), given as one weight [3C][C] (rows 0..C-1 for q, C..2C-1 for
  *     k, 2C..3C-1 for v) and one bias [3C].
+ *   - The block around BRA ("p3" below: "BiFormer架构核心思想解析" §3.1,
+ *     `x = x + self.bra(self.norm1(x))`) normalises each token with
+ *     nn.LayerNorm(dim): over its C channels, biased variance, eps = 1e-5
+ *     (PyTorch's default), then a per-channel scale and shift.
  *
  * All tensors are contiguous channels-last [B, H, W, C] arrays of double.
  * Functions return 0 on success and 1 on an invalid argument.
@@ -413,5 +417,30 @@ int oracle_qkv_project(const double *x, int M, int C, const double *w, const dou
         for (int c = 0; c < C; ++c) acc += x[(size_t)m * C + c] * wr[c];
         outs[t][(size_t)m * C + j] = acc;
       }
+  return ORACLE_OK;
+}
+
+/*
+ * p3 ("BiFormer架构核心思想解析") §3.1, `self.norm1 = nn.LayerNorm(dim)`:
+ * y[m][c] = (x[m][c] - mean_m) / sqrt(var_m + eps) * gamma[c] + beta[c],
+ * with mean_m and var_m (biased: divided by C) over the C channels of token m.
+ * gamma and beta may be NULL (1 and 0).
+ */
+int oracle_layer_norm(const double *x, int M, int C, const double *gamma,
+                      const double *beta, double eps, double *y) {
+  if (!x || !y || M < 0 || C <= 0 || !(eps >= 0.0)) return ORACLE_EINVAL;
+  for (int m = 0; m < M; ++m) {
+    const double *xr = x + (size_t)m * C;
+    double mean = 0.0;
+    for (int c = 0; c < C; ++c) mean += xr[c];
+    mean /= C;
+    double var = 0.0;
+    for (int c = 0; c < C; ++c) var += (xr[c] - mean) * (xr[c] - mean);
+    var /= C;
+    const double rstd = 1.0 / sqrt(var + eps);
+    for (int c = 0; c < C; ++c)
+      y[(size_t)m * C + c] = (xr[c] - mean) * rstd * (gamma ? gamma[c] : 1.0) +
+                             (beta ? beta[c] : 0.0);
+  }
   return ORACLE_OK;
 }

@@ -378,3 +378,58 @@ def test_qkv_projection_special_cases():
     perm = np.eye(8)[::-1]
     q, _, _ = oracle.qkv_project(x, np.concatenate([perm, eye, eye]), None)
     assert np.array_equal(q, x[..., ::-1])
+
+
+# ------------------------------------------------------- block (LayerNorm)
+def test_layer_norm_equals_the_library_routine():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((2, 3, 5, 24)) * 3 + 1.5
+    g, b = rng.standard_normal(24), rng.standard_normal(24)
+    y = oracle.layer_norm(x, g, b)
+    t = torch.nn.functional.layer_norm(torch.from_numpy(x), (24,), torch.from_numpy(g),
+                                       torch.from_numpy(b), 1e-5).numpy()
+    np.testing.assert_allclose(y, t, rtol=0, atol=1e-12)
+
+
+def test_layer_norm_invariants():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((40, 16))
+    y = oracle.layer_norm(x, eps=0.0)
+    # without scale and shift every token has mean 0 and (biased) variance 1
+    np.testing.assert_allclose(y.mean(-1), 0, atol=1e-14)
+    np.testing.assert_allclose((y * y).mean(-1), 1, atol=1e-13)
+    # a positive scale and a shift of a token change nothing
+    np.testing.assert_allclose(oracle.layer_norm(3.5 * x - 2.0, eps=0.0), y, atol=1e-13)
+    # the affine part is applied after the normalisation
+    g, b = rng.standard_normal(16), rng.standard_normal(16)
+    np.testing.assert_allclose(oracle.layer_norm(x, g, b, eps=0.0), y * g + b, atol=1e-13)
+    # a constant token: variance 0, so the output is the shift alone
+    c = np.full((1, 16), 7.0)
+    np.testing.assert_array_equal(oracle.layer_norm(c, g, b), b[None, :])
+
+
+def test_block_attention_composes_the_stages():
+    """y = x + bra(norm1(x)): with a zero LePE and zero projection weights
+    and bias, q = k = v = 0, every logit is 0, the attention averages v = 0,
+    so y = x exactly; and in general it is x plus the forward of the
+    projected normalised tokens."""
+    rng = np.random.default_rng(7)
+    B, H, W, C, heads, S, topk, ks = 2, 8, 8, 16, 2, 2, 2, 3
+    x = rng.standard_normal((B, H, W, C))
+    ln_w, ln_b = rng.standard_normal(C), rng.standard_normal(C)
+    zw, zb = np.zeros((C, ks, ks)), np.zeros(C)
+    y, _, _ = oracle.block_attention(x, ln_w, ln_b, np.zeros((3 * C, C)), None, heads, S, topk,
+                                     zw, zb)
+    np.testing.assert_array_equal(y, x)
+    w_qkv, b_qkv = rng.standard_normal((3 * C, C)) / 4, rng.standard_normal(3 * C)
+    lw, lb = rng.standard_normal((C, ks, ks)) * 0.1, rng.standard_normal(C) * 0.1
+    y, idx, (xn, q, k, v) = oracle.block_attention(x, ln_w, ln_b, w_qkv, b_qkv, heads, S, topk,
+                                                   lw, lb)
+    tn = torch.nn.functional.layer_norm(torch.from_numpy(x), (C,), torch.from_numpy(ln_w),
+                                        torch.from_numpy(ln_b), 1e-5).numpy()
+    full = tn @ w_qkv.T + b_qkv
+    np.testing.assert_allclose(q, full[..., :C], atol=1e-12)
+    np.testing.assert_allclose(v, full[..., 2 * C:], atol=1e-12)
+    out, idx2 = oracle.forward(q, k, v, heads, S, topk, lw, lb)
+    assert np.array_equal(idx, idx2)
+    np.testing.assert_allclose(y - x, out, atol=1e-12)
