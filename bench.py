@@ -153,6 +153,19 @@ def projection_work(wl: bra_synth.Workload) -> dict:
             "alu_flops": 0, "exps": 0}
 
 
+def block_work(wl: bra_synth.Workload) -> dict:
+    """Algorithmic work of the block's attention branch y = x + bra(norm1(x))
+    as its four steps run it: LayerNorm (x read, x_n written), projection (x_n
+    read, q, k, v written, weight read), forward (q, k, v read, out written),
+    residual add (x and out read, y written): 13 M C elements; flops of the
+    projection and the forward."""
+    M, C = wl.B * wl.H * wl.W, wl.C
+    fwd = algorithmic_work(wl)["forward"]
+    return {"bytes": 13 * M * C * 2 + 3 * C * C * 2,
+            "tensor_flops": fwd["tensor_flops"] + 6 * M * C * C,
+            "alu_flops": fwd["alu_flops"], "exps": fwd["exps"]}
+
+
 def peaks(sm_count: int | None = None, sm_mhz: float | None = None) -> dict:
     """Roofline denominators: HBM GB/s and bf16 tensor TFLOP/s measured on
     the B300s (MEASURED_PEAKS.json, burst figures for kernels timed
@@ -498,6 +511,55 @@ def time_projection(wl, dev, stream, steps: int) -> float:
     return ms
 
 
+def time_block(wl, dev, stream, steps: int) -> float:
+    """ms per bra_block_attention call (four launches) on the workload's map,
+    from CUDA graphs over rotating input sets larger than L2."""
+    import numpy as np
+    import torch
+    import vision_transformer_sparse_route_b300 as bra
+    B, H, W, C = wl.B, wl.H, wl.W, wl.C
+    M = B * H * W
+    x, w, b = bra_synth.make_projection_inputs(M, C, 0)
+    rng = np.random.default_rng(0)
+    wd = torch.from_numpy(w).to(torch.bfloat16).to(dev)
+    bd = torch.from_numpy(b).to(dev)
+    lnw = torch.from_numpy((1 + 0.1 * rng.standard_normal(C)).astype(np.float32)).to(dev)
+    lnb = torch.from_numpy((0.1 * rng.standard_normal(C)).astype(np.float32)).to(dev)
+    lw = torch.from_numpy((0.02 * rng.standard_normal((C, wl.ks, wl.ks))).astype(np.float32)).to(dev)
+    lb = torch.from_numpy((0.02 * rng.standard_normal(C)).astype(np.float32)).to(dev)
+    ws_bytes = bra._load().bra_block_attention_workspace_bytes(B, H, W, C, wl.S, wl.topk)
+    per_set = 2 * M * C * 2 + ws_bytes
+    sets = max(2, -(-3 * L2_BYTES // per_set) + 1)
+    xh = torch.from_numpy(x).to(torch.bfloat16).reshape(B, H, W, C)
+    bufs = [(xh.to(dev), torch.empty((B, H, W, C), dtype=torch.bfloat16, device=dev),
+             torch.empty(ws_bytes, dtype=torch.uint8, device=dev)) for _ in range(sets)]
+    def call(xs, y, ws):
+        bra.block_attention(xs, lnw, lnb, wd, bd, wl.heads, wl.S, wl.topk, lw, lb, out=y,
+                            workspace=ws, stream=stream)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for t in bufs:
+            call(*t)
+        stream.synchronize()
+        for t in bufs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(*t)
+            graphs.append(g)
+        for i in range(3):
+            graphs[i % sets].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % sets].replay()
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del graphs, bufs
+    torch.cuda.empty_cache()
+    return ms
+
+
 def launch_floor(torch, stream, reps: int = 2000) -> dict:
     """Replay cost of a CUDA graph holding one near-empty kernel (a
     one-element fill) and one holding two of them in a chain, back to back
@@ -547,9 +609,11 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
         tc_ms = st.time_kernel(st.attend_tc, kernel_steps)
     # the Q/K/V projection that produces this workload's q, k, v (bf16, C a
     # multiple of 64 up to 256)
-    proj_ms = None
+    proj_ms = block_ms = None
     if wl.dtype == "bf16" and wl.C % 64 == 0 and wl.C <= 256:
         proj_ms = time_projection(wl, dev, stream, kernel_steps)
+        # the block's attention branch, x + bra(norm1(x)), projections included
+        block_ms = time_block(wl, dev, stream, kernel_steps)
     work = algorithmic_work(wl)
     ok = st.bra.device_status(stream)
     launches = st.launches()
@@ -566,6 +630,10 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
                  "qkv_project_roofline": roofline(projection_work(wl), pk, wl.dtype,
                                                   proj_ms * 1e-3)}
                 if proj_ms is not None else {}),
+             **({"block_attention_us": block_ms * 1e3,
+                 "block_attention_roofline": roofline(block_work(wl), pk, wl.dtype,
+                                                      block_ms * 1e-3)}
+                if block_ms is not None else {}),
              **({"attend_tc_us": tc_ms * 1e3,
                  "attend_tc_roofline": roofline(work["attend"], pk, wl.dtype, tc_ms * 1e-3)}
                 if tc_ms is not None else {}),

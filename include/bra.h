@@ -187,6 +187,58 @@ int bra_qkv_project(const void *x, const void *w, const float *bias, long long M
                     int dtype, void *q, void *k, void *v, void *stream);
 
 /*
+ * bra_layer_norm -- the LayerNorm of the BiFormer block ("self.norm1 =
+ * nn.LayerNorm(dim)" of the page "BiFormer架构核心思想解析" §3.1) over the C
+ * channels of every token:
+ *   y[m][c] = (x[m][c] - mean_m) / sqrt(var_m + eps) * gamma[c] + beta[c]
+ * with the biased variance; float32 arithmetic, one rounding to bf16.
+ *   x, y     [M][C] device bf16 (y may be x: in place)
+ *   gamma, beta  [C] device float32, or NULL for 1 and 0
+ * Supported: bf16 with C in {64, 128, 256}; otherwise BRA_ERR_UNSUPPORTED.
+ * eps < 0, a NULL or unaligned (16-byte) x or y, or y partly overlapping x:
+ * BRA_ERR_INVALID_ARG. M == 0 enqueues nothing.
+ */
+int bra_layer_norm(const void *x, const float *gamma, const float *beta, long long M, int C,
+                   float eps, int dtype, void *y, void *stream);
+
+/*
+ * bra_residual_add -- y = x + r element by element (the residual of the
+ * same block, "x = x + self.bra(...)"), the float32 sum rounded once to bf16.
+ *   x, r, y  n elements each, device bf16; y may be x or r.
+ * Supported: bf16 with n a multiple of 8; otherwise BRA_ERR_UNSUPPORTED.
+ * NULL or unaligned pointers, or y partly overlapping x or r:
+ * BRA_ERR_INVALID_ARG.
+ */
+int bra_residual_add(const void *x, const void *r, long long n, int dtype, void *y,
+                     void *stream);
+
+/* Bytes of the workspace bra_block_attention needs; 0 on invalid sizes. */
+size_t bra_block_attention_workspace_bytes(int B, int H, int W, int C, int S, int topk);
+
+/*
+ * bra_block_attention -- the attention branch of the BiFormer block (page
+ * "BiFormer架构核心思想解析" §3.1): y = x + bra(norm1(x)), where bra is the
+ * Q/K/V projections of the cybasar page §3 followed by bra_forward (routing,
+ * routed attention and LePE; the pages give BRA no output projection). It
+ * enqueues bra_layer_norm, bra_qkv_project, bra_forward and
+ * bra_residual_add on the stream.
+ *   x         [B, H, W, C] device bf16, the block input
+ *   ln_w, ln_b  LayerNorm scale and shift, [C] float32 (or NULL), eps as in
+ *             bra_layer_norm
+ *   w_qkv, b_qkv  as w and bias of bra_qkv_project
+ *   lepe_*    as in bra_attend
+ *   workspace device buffer of bra_block_attention_workspace_bytes(...) bytes
+ *             (16-byte aligned): the normalised tokens, q, k, v and the
+ *             routing index
+ *   y         out: [B, H, W, C] device bf16, disjoint from x and workspace
+ * Supported: bf16 and the shapes of its four steps; errors as those steps'.
+ */
+int bra_block_attention(const void *x, const float *ln_w, const float *ln_b, float eps,
+                        const void *w_qkv, const float *b_qkv, int B, int H, int W, int C,
+                        int heads, int S, int topk, const float *lepe_w, const float *lepe_b,
+                        int lepe_ks, int dtype, void *workspace, void *y, void *stream);
+
+/*
  * bra_forward_launches -- how many kernels bra_forward (and
  * bra_forward_static) enqueue for this problem on the current device: 1 or 2,
  * 0 for B == 0, or minus a status code for invalid sizes. Nothing is

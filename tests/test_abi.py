@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.bra_abi_version() == 101
+    assert lib.bra_abi_version() == 102
     assert bra.status_string(0) == "ok"
     assert "unsupported" in bra.status_string(2)
     assert bra.status_string(99) == "unknown status"

@@ -159,3 +159,14 @@ def test_workload_selection_and_config_numbers():
     assert bench.CONFIG_NUMBER["tiny_f32"] == 1 and bench.CONFIG_NUMBER["stage3_bf16"] == 4
     args = bench.parse_args([])
     assert args.workload == "stage1_bf16" and args.workloads == "all"
+
+
+def test_block_work_counts_each_step_once():
+    wl = bra_synth.WORKLOADS["stage1_bf16"]
+    M, C = wl.B * wl.H * wl.W, wl.C
+    w = bench.block_work(wl)
+    fwd = bench.algorithmic_work(wl)["forward"]
+    # LayerNorm 2 MC, projection 4 MC, forward 4 MC, residual add 3 MC (bf16)
+    assert w["bytes"] == (2 + 4 + 4 + 3) * M * C * 2 + 3 * C * C * 2
+    assert w["tensor_flops"] == fwd["tensor_flops"] + 2 * M * C * 3 * C
+    assert w["exps"] == fwd["exps"]

@@ -40,6 +40,11 @@ SYMBOLS = {
     "bra_status_string": (ctypes.c_char_p, [_I]),
     "bra_abi_version": (_I, []),
     "bra_check_wait_timeout": (_I, [ctypes.c_uint64, _P]),
+    "bra_layer_norm": (_I, [_P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _I, _P, _P]),
+    "bra_residual_add": (_I, [_P, _P, ctypes.c_longlong, _I, _P, _P]),
+    "bra_block_attention_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "bra_block_attention": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, _I, _I, _I,
+                                 _I, _P, _P, _I, _I, _P, _P, _P]),
 }
 
 _lib = None
@@ -159,6 +164,49 @@ def qkv_project(x, w, bias=None, q=None, k=None, v=None, stream=None):
                                  _ptr(k), _ptr(v), _stream(stream))
     _check(rc, "bra_qkv_project")
     return q, k, v
+
+
+def layer_norm(x, gamma=None, beta=None, eps: float = 1e-5, out=None, stream=None):
+    """nn.LayerNorm over the last axis of a bf16 tensor (gamma, beta float32
+    [C] or None); out may be x."""
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    C = x.shape[-1]
+    out = torch.empty_like(x) if out is None else out
+    rc = _load().bra_layer_norm(_ptr(x), _ptr(gamma), _ptr(beta), x.numel() // C, C, eps,
+                                _dtype_code(x), _ptr(out), _stream(stream))
+    _check(rc, "bra_layer_norm")
+    return out
+
+
+def residual_add(x, r, out=None, stream=None):
+    """x + r (bf16, one rounding); out may be x or r."""
+    if not (x.is_contiguous() and r.is_contiguous()) or x.shape != r.shape:
+        raise ValueError("x and r must be contiguous and of one shape")
+    out = torch.empty_like(x) if out is None else out
+    rc = _load().bra_residual_add(_ptr(x), _ptr(r), x.numel(), _dtype_code(x), _ptr(out),
+                                  _stream(stream))
+    _check(rc, "bra_residual_add")
+    return out
+
+
+def block_attention(x, ln_w, ln_b, w_qkv, b_qkv, heads: int, S: int, topk: int, lepe_w,
+                    lepe_b=None, eps: float = 1e-5, out=None, workspace=None, stream=None):
+    """The attention branch of the BiFormer block: x + bra(norm1(x)), with the
+    Q/K/V projections (w_qkv [3C, C] bf16, b_qkv [3C] float32) inside bra.
+    Returns out [B, H, W, C] bf16."""
+    B, H, W, C = _map(x, "x")
+    lib = _load()
+    if workspace is None:
+        n = lib.bra_block_attention_workspace_bytes(B, H, W, C, S, topk)
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    out = torch.empty_like(x) if out is None else out
+    rc = lib.bra_block_attention(_ptr(x), _ptr(ln_w), _ptr(ln_b), eps, _ptr(w_qkv), _ptr(b_qkv),
+                                 B, H, W, C, heads, S, topk, _ptr(lepe_w), _ptr(lepe_b),
+                                 lepe_w.shape[-1], _dtype_code(x), _ptr(workspace), _ptr(out),
+                                 _stream(stream))
+    _check(rc, "bra_block_attention")
+    return out
 
 
 def attend_tc(q, k, v, idx, heads: int, S: int, lepe_w, lepe_b=None, out=None, stream=None):

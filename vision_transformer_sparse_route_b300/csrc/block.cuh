@@ -1,0 +1,91 @@
+// block.cuh -- the pieces of the BiFormer block's attention branch around
+// BRA (page "BiFormer架构核心思想解析" §3.1: x = x + self.bra(self.norm1(x))):
+// the LayerNorm of every token over its channels and the residual add.
+// Both move each element once (HBM-bound); the arithmetic is float32 with
+// one rounding to bf16.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace bra {
+
+constexpr int kLnThreads = 256;
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// nn.LayerNorm over the C channels of each token: y = (x - mean) / sqrt(var +
+// eps) * gamma + beta, biased variance, computed two-pass from registers.
+// G = C / 8 lanes hold a token (one 16-byte chunk each, G in 8, 16, 32), so a
+// warp normalises 32 / G tokens at once with coalesced loads and stores.
+template <int G>
+__global__ void __launch_bounds__(kLnThreads)
+    bra_layer_norm_kernel(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ gamma,
+                          const float *__restrict__ beta, long long M, float eps,
+                          __nv_bfloat16 *__restrict__ y) {
+  constexpr int C = 8 * G;
+  constexpr int TPW = 32 / G;  // tokens a warp
+  const int lane = threadIdx.x & 31, sub = lane % G;
+  const long long m = ((long long)blockIdx.x * (kLnThreads / 32) + (threadIdx.x >> 5)) * TPW +
+                      lane / G;
+  const bool live = m < M;
+  float v[8];
+  if (live) {
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(x + m * C) + sub), v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  }
+  float s = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+#pragma unroll
+  for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  const float mean = s * (1.0f / C);
+  float d2 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d2 = fmaf(v[i] - mean, v[i] - mean, d2);
+#pragma unroll
+  for (int off = G / 2; off > 0; off >>= 1) d2 += __shfl_xor_sync(0xffffffffu, d2, off);
+  const float rstd = rsqrtf(d2 * (1.0f / C) + eps);
+  if (!live) return;
+  const int c0 = 8 * sub;
+  float o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float gi = gamma ? __ldg(gamma + c0 + i) : 1.f;
+    const float bi = beta ? __ldg(beta + c0 + i) : 0.f;
+    o[i] = fmaf((v[i] - mean) * rstd, gi, bi);
+  }
+  reinterpret_cast<uint4 *>(y + m * C)[sub] =
+      make_uint4(pack2_bf16(o[0], o[1]), pack2_bf16(o[2], o[3]), pack2_bf16(o[4], o[5]),
+                 pack2_bf16(o[6], o[7]));
+}
+
+// y = x + r element by element (n a multiple of 8), float32 sum rounded once
+// to bf16; y may be r.
+__global__ void __launch_bounds__(kLnThreads)
+    bra_residual_add_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *r,
+                            long long n8, __nv_bfloat16 *y) {
+  for (long long i = (long long)blockIdx.x * kLnThreads + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * kLnThreads) {
+    float a[8], b[8];
+    unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(x) + i), a);
+    unpack_bf16x8(reinterpret_cast<const uint4 *>(r)[i], b);
+    reinterpret_cast<uint4 *>(y)[i] =
+        make_uint4(pack2_bf16(a[0] + b[0], a[1] + b[1]), pack2_bf16(a[2] + b[2], a[3] + b[3]),
+                   pack2_bf16(a[4] + b[4], a[5] + b[5]), pack2_bf16(a[6] + b[6], a[7] + b[7]));
+  }
+}
+
+}  // namespace bra

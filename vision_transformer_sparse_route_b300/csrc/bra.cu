@@ -18,6 +18,7 @@
 #include "attend_f32.cuh"
 #include "attend_image.cuh"
 #include "attend_tc.cuh"
+#include "block.cuh"
 #include "qkv_tc.cuh"
 #include "forward_image.cuh"
 #include "route.cuh"
@@ -1042,6 +1043,91 @@ int bra_forward_launches(int B, int H, int W, int C, int heads, int S, int topk,
   return forward_launches(B, H, W, C, heads, S, topk, lepe_ks, dtype);
 }
 
+int bra_layer_norm(const void *x, const float *gamma, const float *beta, long long M, int C,
+                   float eps, int dtype, void *y, void *stream) {
+  if (M < 0 || C <= 0 || !(eps >= 0.f)) return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_F32 && dtype != BRA_BF16) return BRA_ERR_INVALID_ARG;
+  if (M == 0) return BRA_OK;
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return BRA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)M * C * elem_size(dtype);
+  if (x != y && overlap(x, bytes, y, bytes)) return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_BF16 || (C != 64 && C != 128 && C != 256)) return BRA_ERR_UNSUPPORTED;
+  (void)cudaGetLastError();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = C / 8;
+  const long long per_block = (bra::kLnThreads / 32) * (32 / G);
+  const unsigned grid = (unsigned)((M + per_block - 1) / per_block);
+  const auto *xi = static_cast<const __nv_bfloat16 *>(x);
+  auto *yo = static_cast<__nv_bfloat16 *>(y);
+  if (G == 8)
+    bra::bra_layer_norm_kernel<8><<<grid, bra::kLnThreads, 0, s>>>(xi, gamma, beta, M, eps, yo);
+  else if (G == 16)
+    bra::bra_layer_norm_kernel<16><<<grid, bra::kLnThreads, 0, s>>>(xi, gamma, beta, M, eps, yo);
+  else
+    bra::bra_layer_norm_kernel<32><<<grid, bra::kLnThreads, 0, s>>>(xi, gamma, beta, M, eps, yo);
+  return cuda_status(cudaGetLastError());
+}
+
+int bra_residual_add(const void *x, const void *r, long long n, int dtype, void *y,
+                     void *stream) {
+  if (n < 0) return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_F32 && dtype != BRA_BF16) return BRA_ERR_INVALID_ARG;
+  if (n == 0) return BRA_OK;
+  if (!x || !r || !y || !aligned16(x) || !aligned16(r) || !aligned16(y))
+    return BRA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)n * elem_size(dtype);
+  if ((x != y && overlap(x, bytes, y, bytes)) || (r != y && overlap(r, bytes, y, bytes)))
+    return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_BF16 || n % 8) return BRA_ERR_UNSUPPORTED;
+  (void)cudaGetLastError();
+  const long long n8 = n / 8;
+  const unsigned grid = (unsigned)std::min<long long>((n8 + bra::kLnThreads - 1) / bra::kLnThreads,
+                                                      (long long)sm_count() * 8);
+  bra::bra_residual_add_kernel<<<grid, bra::kLnThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(r), n8,
+      static_cast<__nv_bfloat16 *>(y));
+  return cuda_status(cudaGetLastError());
+}
+
+size_t bra_block_attention_workspace_bytes(int B, int H, int W, int C, int S, int topk) {
+  if (B < 0 || H <= 0 || W <= 0 || C <= 0 || S <= 0 || topk <= 0) return 0;
+  // the normalised tokens, q, k and v (bf16), then the routing index
+  return round_up((size_t)4 * B * H * W * C * 2, 256) + bra_idx_workspace_bytes(B, S, topk);
+}
+
+int bra_block_attention(const void *x, const float *ln_w, const float *ln_b, float eps,
+                        const void *w_qkv, const float *b_qkv, int B, int H, int W, int C,
+                        int heads, int S, int topk, const float *lepe_w, const float *lepe_b,
+                        int lepe_ks, int dtype, void *workspace, void *y, void *stream) {
+  int rc = check_map_args(B, H, W, C, S, topk, dtype);
+  if (rc) return rc;
+  if (heads <= 0 || C % heads || lepe_ks <= 0 || lepe_ks % 2 == 0 || !(eps >= 0.f))
+    return BRA_ERR_INVALID_ARG;
+  if (B == 0) return BRA_OK;
+  if (!x || !w_qkv || !lepe_w || !workspace || !y) return BRA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(workspace) || !aligned16(y))
+    return BRA_ERR_INVALID_ARG;
+  const size_t mc = (size_t)B * H * W * C;
+  const size_t bytes = mc * elem_size(dtype);
+  const size_t ws = bra_block_attention_workspace_bytes(B, H, W, C, S, topk);
+  if (overlap(y, bytes, x, bytes) || overlap(y, bytes, workspace, ws) ||
+      overlap(x, bytes, workspace, ws))
+    return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_BF16) return BRA_ERR_UNSUPPORTED;
+  uint8_t *w8 = static_cast<uint8_t *>(workspace);
+  void *xn = w8, *q = w8 + 2 * mc, *k = w8 + 4 * mc, *v = w8 + 6 * mc;
+  int32_t *idx = reinterpret_cast<int32_t *>(w8 + round_up(8 * mc, 256));
+  const long long M = (long long)B * H * W;
+  rc = bra_layer_norm(x, ln_w, ln_b, M, C, eps, dtype, xn, stream);
+  if (rc) return rc;
+  rc = bra_qkv_project(xn, w_qkv, b_qkv, M, C, dtype, q, k, v, stream);
+  if (rc) return rc;
+  rc = bra_forward(q, k, v, B, H, W, C, heads, S, topk, lepe_w, lepe_b, lepe_ks, dtype, idx, y,
+                   stream);
+  if (rc) return rc;
+  return bra_residual_add(x, y, (long long)mc, dtype, y, stream);
+}
+
 size_t bra_idx_workspace_bytes(int B, int S, int topk) {
   if (B < 0 || S <= 0 || topk <= 0) return 0;
   return (size_t)B * S * S * topk * sizeof(int32_t);
@@ -1074,7 +1160,7 @@ const char *bra_status_string(int status) {
   }
 }
 
-int bra_abi_version(void) { return 101; }
+int bra_abi_version(void) { return 102; }
 
 int bra_check_wait_timeout(uint64_t limit_ns, void *stream) {
   if (limit_ns < 1000 || limit_ns > 1000000000ull) return BRA_ERR_INVALID_ARG;
