@@ -49,6 +49,8 @@ def _load():
             "oracle_forward": [P, P, P, I, I, I, I, I, I, I, P, P, I, P, P, I],
             "oracle_qkv_project": [P, I, I, P, P, P, P, P],
             "oracle_layer_norm": [P, I, I, P, P, ctypes.c_double, P],
+            "oracle_linear": [P, I, I, P, I, P, P],
+            "oracle_gelu": [P, ctypes.c_size_t, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -209,3 +211,40 @@ def block_attention(x, ln_w, ln_b, w_qkv, b_qkv, heads: int, S: int, topk: int, 
     q, k, v = qkv_project(xn, w_qkv, b_qkv)
     out, idx = forward(q, k, v, heads, S, topk, lepe_w, lepe_b, threads=threads)
     return x + out, idx, (xn, q, k, v)
+
+
+def linear(x, w, bias=None) -> np.ndarray:
+    """nn.Linear over the last axis: x [..., K], w [N, K], bias [N] or None."""
+    x, w = _f64(x), _f64(w)
+    bias = None if bias is None else _f64(bias)
+    K = x.shape[-1]
+    N = w.shape[0]
+    if w.shape != (N, K):
+        raise ValueError("w must be [N, K]")
+    M = int(np.prod(x.shape[:-1]))
+    y = np.empty(x.shape[:-1] + (N,))
+    _check(_load().oracle_linear(_p(x), M, K, _p(w), N, _p(bias), _p(y)), "linear")
+    return y
+
+
+def gelu(x) -> np.ndarray:
+    """nn.GELU, exact (erf) form."""
+    x = _f64(x)
+    y = np.empty_like(x)
+    _check(_load().oracle_gelu(_p(x), x.size, _p(y)), "gelu")
+    return y
+
+
+def block_ffn(x, ln_w, ln_b, w1, b1, conv_w, conv_b, w2, b2, eps: float = 1e-5):
+    """The ConvFFN branch of the BiFormer block (p3 "BiFormer架构核心思想解析"
+    §3.1 `x = x + self.ffn(self.norm2(x))`; p1 §4 ratio 3): y = x +
+    fc2(GELU(dwconv3x3(fc1(norm2(x))))). x [B, H, W, C]; w1 [3C, C]; conv_w
+    [3C, 3, 3], conv_b [3C] (the depthwise convolution, zero padding 1, the
+    same operation as the LePE's); w2 [C, 3C]. Returns (y, the stages: x_n,
+    fc1 output, convolved, activated)."""
+    x = _f64(x)
+    xn = layer_norm(x, ln_w, ln_b, eps)
+    h = linear(xn, w1, b1)
+    hc = lepe(h, conv_w, conv_b)
+    ha = gelu(hc)
+    return x + linear(ha, w2, b2), (xn, h, hc, ha)

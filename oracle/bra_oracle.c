@@ -45,6 +45,11 @@
  *     `x = x + self.bra(self.norm1(x))`) normalises each token with
  *     nn.LayerNorm(dim): over its C channels, biased variance, eps = 1e-5
  *     (PyTorch's default), then a per-channel scale and shift.
+ *   - Its ConvFFN (p3 §3.1 "ConvFFN: a feed-forward network with a 3x3
+ *     depthwise convolution"; p1 §4: a two-layer MLP of ratio 3) is read as
+ *     fc2(GELU(dwconv3x3(fc1(x)))): fc1 = Linear(C, 3C), a depthwise 3x3
+ *     convolution with bias and zero padding 1 in the 3C-channel hidden
+ *     layer, the exact (erf) GELU of nn.GELU, fc2 = Linear(3C, C).
  *
  * All tensors are contiguous channels-last [B, H, W, C] arrays of double.
  * Functions return 0 on success and 1 on an invalid argument.
@@ -442,5 +447,30 @@ int oracle_layer_norm(const double *x, int M, int C, const double *gamma,
       y[(size_t)m * C + c] = (xr[c] - mean) * rstd * (gamma ? gamma[c] : 1.0) +
                              (beta ? beta[c] : 0.0);
   }
+  return ORACLE_OK;
+}
+
+/*
+ * A linear layer (nn.Linear): y[m][n] = sum_k x[m][k] w[n][k] + bias[n]
+ * (bias may be NULL); x [M][K], w [N][K], y [M][N]. Used for the ConvFFN's
+ * fc1 and fc2 (p3 §3.1, p1 §4).
+ */
+int oracle_linear(const double *x, int M, int K, const double *w, int N, const double *bias,
+                  double *y) {
+  if (!x || !w || !y || M < 0 || K <= 0 || N <= 0) return ORACLE_EINVAL;
+  for (int m = 0; m < M; ++m)
+    for (int n = 0; n < N; ++n) {
+      double acc = bias ? bias[n] : 0.0;
+      const double *wr = w + (size_t)n * K;
+      for (int k = 0; k < K; ++k) acc += x[(size_t)m * K + k] * wr[k];
+      y[(size_t)m * N + n] = acc;
+    }
+  return ORACLE_OK;
+}
+
+/* nn.GELU (exact form): x * (1 + erf(x / sqrt 2)) / 2, element by element. */
+int oracle_gelu(const double *x, size_t n, double *y) {
+  if (!x || !y) return ORACLE_EINVAL;
+  for (size_t i = 0; i < n; ++i) y[i] = 0.5 * x[i] * (1.0 + erf(x[i] / sqrt(2.0)));
   return ORACLE_OK;
 }

@@ -433,3 +433,45 @@ def test_block_attention_composes_the_stages():
     out, idx2 = oracle.forward(q, k, v, heads, S, topk, lw, lb)
     assert np.array_equal(idx, idx2)
     np.testing.assert_allclose(y - x, out, atol=1e-12)
+
+
+# ------------------------------------------------------- block (ConvFFN)
+def test_linear_and_gelu_equal_library_routines():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((3, 4, 10))
+    w, b = rng.standard_normal((7, 10)), rng.standard_normal(7)
+    np.testing.assert_allclose(oracle.linear(x, w, b), np.einsum("abk,nk->abn", x, w) + b,
+                               rtol=0, atol=1e-12)
+    t = torch.from_numpy(x * 3)
+    np.testing.assert_allclose(oracle.gelu(x * 3), torch.nn.functional.gelu(t).numpy(),
+                               rtol=0, atol=1e-12)
+    # GELU(x) - GELU(-x) = x (erf is odd), GELU(0) = 0, GELU(x) -> x for large x
+    g = oracle.gelu(x) - oracle.gelu(-x)
+    np.testing.assert_allclose(g, x, atol=1e-14)
+    assert oracle.gelu(np.zeros(3)).tolist() == [0.0, 0.0, 0.0]
+    np.testing.assert_allclose(oracle.gelu(np.array([40.0])), [40.0], rtol=0, atol=1e-12)
+
+
+def test_block_ffn_composes_the_stages():
+    """y = x + fc2(GELU(dwconv(fc1(norm2(x))))): zero fc2 weight and bias give
+    y = x exactly; in general the stages equal torch's layer_norm, linear,
+    depthwise conv2d and gelu applied in that order."""
+    rng = np.random.default_rng(13)
+    B, H, W, C = 2, 6, 5, 8
+    x = rng.standard_normal((B, H, W, C))
+    ln_w, ln_b = rng.standard_normal(C), rng.standard_normal(C)
+    w1, b1 = rng.standard_normal((3 * C, C)) / 3, rng.standard_normal(3 * C)
+    cw, cb = rng.standard_normal((3 * C, 3, 3)) / 3, rng.standard_normal(3 * C)
+    w2, b2 = rng.standard_normal((C, 3 * C)) / 5, rng.standard_normal(C)
+    y, _ = oracle.block_ffn(x, ln_w, ln_b, w1, b1, cw, cb, np.zeros((C, 3 * C)), None)
+    np.testing.assert_array_equal(y, x)
+    y, (xn, h, hc, ha) = oracle.block_ffn(x, ln_w, ln_b, w1, b1, cw, cb, w2, b2)
+    F = torch.nn.functional
+    tx = torch.from_numpy(x)
+    tn = F.layer_norm(tx, (C,), torch.from_numpy(ln_w), torch.from_numpy(ln_b), 1e-5)
+    th = F.linear(tn, torch.from_numpy(w1), torch.from_numpy(b1))
+    tc = F.conv2d(th.permute(0, 3, 1, 2), torch.from_numpy(cw)[:, None], torch.from_numpy(cb),
+                  padding=1, groups=3 * C).permute(0, 2, 3, 1)
+    ty = tx + F.linear(F.gelu(tc), torch.from_numpy(w2), torch.from_numpy(b2))
+    np.testing.assert_allclose(hc, tc.numpy(), atol=1e-12)
+    np.testing.assert_allclose(y, ty.numpy(), atol=1e-12)
