@@ -166,6 +166,17 @@ def block_work(wl: bra_synth.Workload) -> dict:
             "alu_flops": fwd["alu_flops"], "exps": fwd["exps"]}
 
 
+def ffn_work(wl: bra_synth.Workload) -> dict:
+    """Algorithmic work of the block's ConvFFN branch y = x + fc2(GELU(
+    dwconv3x3(fc1(norm2(x))))) as its four steps run it: LayerNorm 2 M C,
+    fc1 M C + 3 M C, the convolution and GELU 3 M C + 3 M C, fc2 3 M C + M C
+    (residual) + M C elements (bf16), the weights once; contraction flops of
+    fc1 and fc2, float32 flops of the 3 x 3 convolution."""
+    M, C = wl.B * wl.H * wl.W, wl.C
+    return {"bytes": 17 * M * C * 2 + 2 * 3 * C * C * 2 + 10 * 3 * C * 4,
+            "tensor_flops": 2 * 6 * M * C * C, "alu_flops": 2 * 9 * 3 * M * C, "exps": 0}
+
+
 def peaks(sm_count: int | None = None, sm_mhz: float | None = None) -> dict:
     """Roofline denominators: HBM GB/s and bf16 tensor TFLOP/s measured on
     the B300s (MEASURED_PEAKS.json, burst figures for kernels timed
@@ -560,6 +571,55 @@ def time_block(wl, dev, stream, steps: int) -> float:
     return ms
 
 
+def time_block_ffn(wl, dev, stream, steps: int) -> float:
+    """ms per bra_block_ffn call (four launches) on the workload's map, from
+    CUDA graphs over rotating input sets larger than L2."""
+    import numpy as np
+    import torch
+    import vision_transformer_sparse_route_b300 as bra
+    B, H, W, C = wl.B, wl.H, wl.W, wl.C
+    M = B * H * W
+    rng = np.random.default_rng(1)
+    d = lambda a, t=torch.float32: torch.from_numpy(a.astype(np.float32)).to(t).to(dev)  # noqa
+    lnw, lnb = d(1 + 0.1 * rng.standard_normal(C)), d(0.1 * rng.standard_normal(C))
+    w1 = d(rng.standard_normal((3 * C, C)) / np.sqrt(C), torch.bfloat16)
+    b1 = d(0.02 * rng.standard_normal(3 * C))
+    cw, cb = d(rng.standard_normal((3 * C, 3, 3)) / 3), d(0.02 * rng.standard_normal(3 * C))
+    w2 = d(rng.standard_normal((C, 3 * C)) / np.sqrt(3 * C), torch.bfloat16)
+    b2 = d(0.02 * rng.standard_normal(C))
+    ws_bytes = bra._load().bra_block_ffn_workspace_bytes(B, H, W, C)
+    per_set = 2 * M * C * 2 + ws_bytes
+    sets = max(2, -(-3 * L2_BYTES // per_set) + 1)
+    x, _, _ = bra_synth.make_projection_inputs(M, C, 0)
+    xh = torch.from_numpy(x).to(torch.bfloat16).reshape(B, H, W, C)
+    bufs = [(xh.to(dev), torch.empty((B, H, W, C), dtype=torch.bfloat16, device=dev),
+             torch.empty(ws_bytes, dtype=torch.uint8, device=dev)) for _ in range(sets)]
+    def call(xs, y, ws):
+        bra.block_ffn(xs, lnw, lnb, w1, b1, cw, cb, w2, b2, out=y, workspace=ws, stream=stream)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for t in bufs:
+            call(*t)
+        stream.synchronize()
+        for t in bufs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(*t)
+            graphs.append(g)
+        for i in range(3):
+            graphs[i % sets].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % sets].replay()
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del graphs, bufs
+    torch.cuda.empty_cache()
+    return ms
+
+
 def launch_floor(torch, stream, reps: int = 2000) -> dict:
     """Replay cost of a CUDA graph holding one near-empty kernel (a
     one-element fill) and one holding two of them in a chain, back to back
@@ -614,6 +674,10 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
         proj_ms = time_projection(wl, dev, stream, kernel_steps)
         # the block's attention branch, x + bra(norm1(x)), projections included
         block_ms = time_block(wl, dev, stream, kernel_steps)
+    ffn_ms = None
+    if wl.dtype == "bf16" and wl.C in (64, 128):
+        # the block's ConvFFN branch (its fc2 takes K = 3C up to 384)
+        ffn_ms = time_block_ffn(wl, dev, stream, kernel_steps)
     work = algorithmic_work(wl)
     ok = st.bra.device_status(stream)
     launches = st.launches()
@@ -634,6 +698,9 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
                  "block_attention_roofline": roofline(block_work(wl), pk, wl.dtype,
                                                       block_ms * 1e-3)}
                 if block_ms is not None else {}),
+             **({"block_ffn_us": ffn_ms * 1e3,
+                 "block_ffn_roofline": roofline(ffn_work(wl), pk, wl.dtype, ffn_ms * 1e-3)}
+                if ffn_ms is not None else {}),
              **({"attend_tc_us": tc_ms * 1e3,
                  "attend_tc_roofline": roofline(work["attend"], pk, wl.dtype, tc_ms * 1e-3)}
                 if tc_ms is not None else {}),

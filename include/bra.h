@@ -212,6 +212,59 @@ int bra_layer_norm(const void *x, const float *gamma, const float *beta, long lo
 int bra_residual_add(const void *x, const void *r, long long n, int dtype, void *y,
                      void *stream);
 
+/*
+ * bra_linear -- a linear layer (nn.Linear) on the tensor cores, the kernel of
+ * bra_qkv_project with one output: y[m][n] = sum_k x[m][k] w[n][k] + bias[n]
+ * (+ residual[m][n] when residual is not NULL), f32 accumulation, one
+ * rounding to bf16. The ConvFFN's fc1 and fc2 (page "BiFormer架构核心思想解析"
+ * §3.1; the cybasar page §4: ratio 3).
+ *   x [M][K], w [N][K] device bf16; bias [N] device float32 or NULL;
+ *   residual [M][N] device bf16 or NULL (it may be y); y [M][N] device bf16.
+ * Supported: bf16, K and N multiples of 64 whose tiles fit in shared memory
+ * (K up to 384 with N = 64 or 128; K up to 256 with N up to 768); otherwise
+ * BRA_ERR_UNSUPPORTED. NULL or unaligned (16-byte) pointers, y overlapping x
+ * or w, or partly overlapping residual: BRA_ERR_INVALID_ARG.
+ */
+int bra_linear(const void *x, const void *w, const float *bias, long long M, int K, int N,
+               const void *residual, int dtype, void *y, void *stream);
+
+/*
+ * bra_dwconv_gelu -- the hidden layer of the ConvFFN: y = GELU(dwconv3x3(h)),
+ * the depthwise 3 x 3 cross-correlation with a bias and zero padding 1 at the
+ * image border (the LePE's operation with a 3 x 3 kernel), then GELU in its
+ * exact form x (1 + erf(x / sqrt 2)) / 2; float32 arithmetic, one rounding.
+ *   h, y      [B, H, W, Ch] device bf16 (disjoint)
+ *   w         [Ch, 3, 3] device float32; bias [Ch] device float32 or NULL
+ * Supported: bf16, Ch a multiple of 8 up to 384 (the hidden layer of
+ * C = 64 or 128; a block holds all channels of an 8-token tile row);
+ * otherwise BRA_ERR_UNSUPPORTED.
+ */
+int bra_dwconv_gelu(const void *h, const float *w, const float *bias, int B, int H, int W,
+                    int Ch, int dtype, void *y, void *stream);
+
+/* Bytes of the workspace bra_block_ffn needs; 0 on invalid sizes. */
+size_t bra_block_ffn_workspace_bytes(int B, int H, int W, int C);
+
+/*
+ * bra_block_ffn -- the ConvFFN branch of the BiFormer block (page
+ * "BiFormer架构核心思想解析" §3.1 "x = x + self.ffn(self.norm2(x))"):
+ *   y = x + fc2(GELU(dwconv3x3(fc1(norm2(x)))))
+ * with fc1 [3C][C] (w1, b1), the convolution [3C, 3, 3] (conv_w, conv_b) and
+ * fc2 [C][3C] (w2, b2). The pages name a two-layer MLP of ratio 3 with a 3 x 3
+ * depthwise convolution; this library reads the convolution as sitting in
+ * the hidden layer before the activation, and the activation as nn.GELU.
+ * It enqueues bra_layer_norm, bra_linear, bra_dwconv_gelu and bra_linear
+ * (with x as the residual).
+ *   x, y      [B, H, W, C] device bf16 (disjoint)
+ *   workspace device buffer of bra_block_ffn_workspace_bytes(...) bytes
+ * Supported: bf16 and the shapes of its steps (C = 64 or 128); errors as
+ * those steps'.
+ */
+int bra_block_ffn(const void *x, const float *ln_w, const float *ln_b, float eps, const void *w1,
+                  const float *b1, const float *conv_w, const float *conv_b, const void *w2,
+                  const float *b2, int B, int H, int W, int C, int dtype, void *workspace,
+                  void *y, void *stream);
+
 /* Bytes of the workspace bra_block_attention needs; 0 on invalid sizes. */
 size_t bra_block_attention_workspace_bytes(int B, int H, int W, int C, int S, int topk);
 

@@ -170,3 +170,12 @@ def test_block_work_counts_each_step_once():
     assert w["bytes"] == (2 + 4 + 4 + 3) * M * C * 2 + 3 * C * C * 2
     assert w["tensor_flops"] == fwd["tensor_flops"] + 2 * M * C * 3 * C
     assert w["exps"] == fwd["exps"]
+
+
+def test_ffn_work_counts_each_step_once():
+    wl = bra_synth.WORKLOADS["stage2_bf16"]
+    M, C = wl.B * wl.H * wl.W, wl.C
+    w = bench.ffn_work(wl)
+    # LayerNorm 2, fc1 4, convolution + GELU 6, fc2 5 (M C elements, bf16)
+    assert w["bytes"] == 17 * M * C * 2 + 2 * 3 * C * C * 2 + 10 * 3 * C * 4
+    assert w["tensor_flops"] == 2 * (2 * M * C * 3 * C)

@@ -29,6 +29,13 @@ def ln_bound(ref: np.ndarray) -> np.ndarray:
     return 2.0 ** -8 * np.abs(ref) + 1e-4
 
 
+def linear_bound(ref: np.ndarray) -> np.ndarray:
+    # one bf16 rounding of the output (half an ulp, 2^-9 relative; twice
+    # that as the bound) plus the float32 accumulation of at most 384
+    # products of unit-size terms
+    return 2.0 ** -8 * np.abs(ref) + 1e-3
+
+
 @pytest.mark.parametrize("C", [64, 128, 256])
 def test_layer_norm_matches_oracle(C, cuda_device):
     rng = np.random.default_rng(C)
@@ -113,3 +120,78 @@ def test_block_attention_step_by_step(wl, cuda_device):
                         inp.lepe_b)
     assert np.abs(f64(out) - att).max() <= TOL["bf16"]
     assert torch.equal(y2, (x.float() + out.float()).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("M,K,N,with_res", [(300, 64, 192, False), (257, 192, 64, True),
+                                            (130, 384, 64, True), (200, 128, 384, False),
+                                            (129, 384, 128, True)])
+def test_linear_matches_oracle(M, K, N, with_res, cuda_device):
+    rng = np.random.default_rng(M + K + N)
+    x = bf16(rng.standard_normal((M, K)), cuda_device)
+    w = bf16(rng.standard_normal((N, K)) / np.sqrt(K), cuda_device)
+    b = (0.1 * rng.standard_normal(N)).astype(np.float32)
+    res = bf16(rng.standard_normal((M, N)) * 2, cuda_device) if with_res else None
+    y = bra.linear(x, w, torch.from_numpy(b).to(cuda_device), residual=res)
+    ref = oracle.linear(f64(x), f64(w), b) + (f64(res) if with_res else 0)
+    assert np.all(np.abs(f64(y) - ref) <= linear_bound(ref))
+    if with_res:  # in place on the residual
+        r2 = res.clone()
+        bra.linear(x, w, torch.from_numpy(b).to(cuda_device), residual=r2, out=r2)
+        assert torch.equal(r2, y)
+
+
+def test_dwconv_gelu_matches_oracle(cuda_device):
+    rng = np.random.default_rng(21)
+    h = bf16(rng.standard_normal((2, 7, 9, 192)), cuda_device)  # ragged map, 3C channels
+    w = (rng.standard_normal((192, 3, 3)) / 3).astype(np.float32)
+    b = (0.1 * rng.standard_normal(192)).astype(np.float32)
+    y = bra.dwconv_gelu(h, torch.from_numpy(w).to(cuda_device), torch.from_numpy(b).to(cuda_device))
+    ref = oracle.gelu(oracle.lepe(f64(h), w, b))
+    assert np.all(np.abs(f64(y) - ref) <= ln_bound(ref))
+
+
+FFN_SHAPES = [Workload("ffn_c64", 2, 16, 16, 64, 2, 2, 2, 5, "bf16"),
+              Workload("ffn_c128_ragged", 1, 14, 10, 128, 4, 2, 2, 5, "bf16")]
+
+
+@pytest.mark.parametrize("wl", FFN_SHAPES, ids=lambda w: w.name)
+def test_block_ffn_step_by_step(wl, cuda_device):
+    rng = np.random.default_rng(31)
+    C = wl.C
+    x = bf16(bra_synth.make_inputs(wl, seed=6).q, cuda_device)
+    ln_w = (1 + 0.1 * rng.standard_normal(C)).astype(np.float32)
+    ln_b = (0.1 * rng.standard_normal(C)).astype(np.float32)
+    w1 = bf16(rng.standard_normal((3 * C, C)) / np.sqrt(C), cuda_device)
+    b1 = (0.02 * rng.standard_normal(3 * C)).astype(np.float32)
+    cw = (rng.standard_normal((3 * C, 3, 3)) / 3).astype(np.float32)
+    cb = (0.02 * rng.standard_normal(3 * C)).astype(np.float32)
+    w2 = bf16(rng.standard_normal((C, 3 * C)) / np.sqrt(3 * C), cuda_device)
+    b2 = (0.02 * rng.standard_normal(C)).astype(np.float32)
+    d = lambda a: torch.from_numpy(a).to(cuda_device)  # noqa: E731
+    y = bra.block_ffn(x, d(ln_w), d(ln_b), w1, d(b1), d(cw), d(cb), w2, d(b2))
+    # the four steps one by one give the same bits
+    xn = bra.layer_norm(x, d(ln_w), d(ln_b))
+    h = bra.linear(xn, w1, d(b1))
+    ha = bra.dwconv_gelu(h, d(cw), d(cb))
+    y2 = bra.linear(ha, w2, d(b2), residual=x)
+    assert bra.device_status() == bra.BRA_OK
+    assert torch.equal(y, y2)
+    # each step against the oracle on that step's GPU input
+    ref = oracle.layer_norm(f64(x), ln_w, ln_b)
+    assert np.all(np.abs(f64(xn) - ref) <= ln_bound(ref))
+    ref = oracle.linear(f64(xn), f64(w1), b1)
+    assert np.all(np.abs(f64(h) - ref) <= linear_bound(ref))
+    ref = oracle.gelu(oracle.lepe(f64(h), cw, cb))
+    assert np.all(np.abs(f64(ha) - ref) <= ln_bound(ref))
+    ref = f64(x) + oracle.linear(f64(ha), f64(w2), b2)
+    assert np.all(np.abs(f64(y2) - ref) <= linear_bound(ref))
+
+
+def test_block_ffn_rejects_wide_channels(cuda_device):
+    C = 256
+    x = torch.zeros((1, 8, 8, C), dtype=torch.bfloat16, device=cuda_device)
+    z = lambda *s: torch.zeros(s, device=cuda_device)  # noqa: E731
+    wb = lambda *s: torch.zeros(s, dtype=torch.bfloat16, device=cuda_device)  # noqa: E731
+    with pytest.raises(bra.BraError):
+        bra.block_ffn(x, None, None, wb(3 * C, C), None, z(3 * C, 3, 3), None, wb(C, 3 * C),
+                      None)

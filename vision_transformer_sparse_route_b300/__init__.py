@@ -43,6 +43,11 @@ SYMBOLS = {
     "bra_layer_norm": (_I, [_P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _I, _P, _P]),
     "bra_residual_add": (_I, [_P, _P, ctypes.c_longlong, _I, _P, _P]),
     "bra_block_attention_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "bra_linear": (_I, [_P, _P, _P, ctypes.c_longlong, _I, _I, _P, _I, _P, _P]),
+    "bra_dwconv_gelu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "bra_block_ffn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "bra_block_ffn": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                           _I, _P, _P, _P]),
     "bra_block_attention": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, _I, _I, _I,
                                  _I, _P, _P, _I, _I, _P, _P, _P]),
 }
@@ -206,6 +211,50 @@ def block_attention(x, ln_w, ln_b, w_qkv, b_qkv, heads: int, S: int, topk: int, 
                                  lepe_w.shape[-1], _dtype_code(x), _ptr(workspace), _ptr(out),
                                  _stream(stream))
     _check(rc, "bra_block_attention")
+    return out
+
+
+def linear(x, w, bias=None, residual=None, out=None, stream=None):
+    """x W^T + bias (+ residual) over the last axis: x [..., K] bf16, w [N, K]
+    bf16, bias [N] float32 or None, residual [..., N] bf16 or None."""
+    if not x.is_contiguous() or not w.is_contiguous():
+        raise ValueError("x and w must be contiguous")
+    K, N = x.shape[-1], w.shape[0]
+    M = x.numel() // K
+    out = torch.empty(x.shape[:-1] + (N,), dtype=x.dtype, device=x.device) if out is None \
+        else out
+    rc = _load().bra_linear(_ptr(x), _ptr(w), _ptr(bias), M, K, N, _ptr(residual),
+                            _dtype_code(x), _ptr(out), _stream(stream))
+    _check(rc, "bra_linear")
+    return out
+
+
+def dwconv_gelu(h, w, bias=None, out=None, stream=None):
+    """GELU(depthwise 3x3 conv of h [B, H, W, Ch] bf16 with w [Ch, 3, 3] and
+    bias [Ch] float32, zero padding 1)."""
+    B, H, W, Ch = _map(h, "h")
+    out = torch.empty_like(h) if out is None else out
+    rc = _load().bra_dwconv_gelu(_ptr(h), _ptr(w), _ptr(bias), B, H, W, Ch, _dtype_code(h),
+                                 _ptr(out), _stream(stream))
+    _check(rc, "bra_dwconv_gelu")
+    return out
+
+
+def block_ffn(x, ln_w, ln_b, w1, b1, conv_w, conv_b, w2, b2, eps: float = 1e-5, out=None,
+              workspace=None, stream=None):
+    """The ConvFFN branch of the BiFormer block: x + fc2(GELU(dwconv3x3(fc1(
+    norm2(x))))); w1 [3C, C], w2 [C, 3C] bf16, conv_w [3C, 3, 3] and the
+    biases float32."""
+    B, H, W, C = _map(x, "x")
+    lib = _load()
+    if workspace is None:
+        workspace = torch.empty(lib.bra_block_ffn_workspace_bytes(B, H, W, C), dtype=torch.uint8,
+                                device=x.device)
+    out = torch.empty_like(x) if out is None else out
+    rc = lib.bra_block_ffn(_ptr(x), _ptr(ln_w), _ptr(ln_b), eps, _ptr(w1), _ptr(b1),
+                           _ptr(conv_w), _ptr(conv_b), _ptr(w2), _ptr(b2), B, H, W, C,
+                           _dtype_code(x), _ptr(workspace), _ptr(out), _stream(stream))
+    _check(rc, "bra_block_ffn")
     return out
 
 

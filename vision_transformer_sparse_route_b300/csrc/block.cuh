@@ -1,8 +1,9 @@
-// block.cuh -- the pieces of the BiFormer block's attention branch around
-// BRA (page "BiFormer架构核心思想解析" §3.1: x = x + self.bra(self.norm1(x))):
-// the LayerNorm of every token over its channels and the residual add.
-// Both move each element once (HBM-bound); the arithmetic is float32 with
-// one rounding to bf16.
+// block.cuh -- the element-wise pieces of the BiFormer block around BRA (page
+// "BiFormer架构核心思想解析" §3.1: x = x + self.bra(self.norm1(x)), then
+// x = x + self.ffn(self.norm2(x))): the LayerNorm of every token over its
+// channels, the residual add, and the ConvFFN's depthwise 3 x 3 convolution
+// with the GELU after it. Each moves its data once (HBM-bound); the
+// arithmetic is float32 with one rounding to bf16.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -85,6 +86,74 @@ __global__ void __launch_bounds__(kLnThreads)
     reinterpret_cast<uint4 *>(y)[i] =
         make_uint4(pack2_bf16(a[0] + b[0], a[1] + b[1]), pack2_bf16(a[2] + b[2], a[3] + b[3]),
                    pack2_bf16(a[4] + b[4], a[5] + b[5]), pack2_bf16(a[6] + b[6], a[7] + b[7]));
+  }
+}
+
+// The ConvFFN's hidden layer: y = GELU(dwconv3x3(h) + bias) over Ch channels
+// (Ch a multiple of 8), the depthwise 3 x 3 cross-correlation zero-padded by 1
+// at the image border, GELU in its exact form x (1 + erf(x / sqrt 2)) / 2.
+// A block takes an 8 x 8 tile of tokens (clipped at the image edge) and all
+// channels: thread (chunk j, column cx) holds the 9 taps of its 8 channels in
+// registers and slides down the tile's 8 rows, so each input it loads (10
+// rows x 3 columns) feeds up to three outputs, and consecutive threads read
+// and write consecutive 16-byte chunks of a token.
+constexpr int kDwTile = 8;
+constexpr int kDwMaxThreads = 384;  // Ch / 8 chunks x 8 columns, Ch up to 384
+
+__global__ void __launch_bounds__(kDwMaxThreads, 1)
+    bra_dwconv_gelu_kernel(const __nv_bfloat16 *__restrict__ h, const float *__restrict__ w,
+                           const float *__restrict__ bias, int B, int H, int W, int Ch,
+                           __nv_bfloat16 *__restrict__ y) {
+  const int nch = Ch / 8;
+  const int j = threadIdx.x % nch, cx = threadIdx.x / nch;  // chunk, tile column
+  const int tiles_x = (W + kDwTile - 1) / kDwTile, tiles_y = (H + kDwTile - 1) / kDwTile;
+  const int tile = blockIdx.x, b = tile / (tiles_x * tiles_y);
+  const int x0 = (tile % tiles_x) * kDwTile, y0 = ((tile / tiles_x) % tiles_y) * kDwTile;
+  const int x = x0 + cx;
+  if (cx >= kDwTile || x >= W || b >= B) return;
+  const int c0 = 8 * j;
+  float wt[9][8], acc[kDwTile][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int tap = 0; tap < 9; ++tap) wt[tap][i] = __ldg(w + (size_t)(c0 + i) * 9 + tap);
+    const float bi = bias ? __ldg(bias + c0 + i) : 0.f;
+#pragma unroll
+    for (int r = 0; r < kDwTile; ++r) acc[r][i] = bi;
+  }
+  const __nv_bfloat16 *hb = h + (size_t)b * H * W * Ch + c0;
+  // input row y0 - 1 + ir feeds output rows ir - dy (dy = 0, 1, 2)
+#pragma unroll
+  for (int ir = 0; ir < kDwTile + 2; ++ir) {
+    const int sy = y0 - 1 + ir;
+    if (sy < 0 || sy >= H) continue;
+#pragma unroll
+    for (int dx = 0; dx < 3; ++dx) {
+      const int sx = x + dx - 1;
+      if (sx < 0 || sx >= W) continue;
+      float v[8];
+      unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(hb + ((size_t)sy * W + sx) * Ch)), v);
+#pragma unroll
+      for (int dy = 0; dy < 3; ++dy) {
+        const int r = ir - dy;
+        if (r < 0 || r >= kDwTile) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[r][i] = fmaf(wt[dy * 3 + dx][i], v[i], acc[r][i]);
+      }
+    }
+  }
+  __nv_bfloat16 *yb = y + (size_t)b * H * W * Ch + c0;
+#pragma unroll
+  for (int r = 0; r < kDwTile; ++r) {
+    const int oy = y0 + r;
+    if (oy >= H) break;
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      o[i] = 0.5f * acc[r][i] * (1.0f + erff(acc[r][i] * 0.70710678118654752f));
+    reinterpret_cast<uint4 *>(yb + ((size_t)oy * W + x) * Ch)[0] =
+        make_uint4(pack2_bf16(o[0], o[1]), pack2_bf16(o[2], o[3]), pack2_bf16(o[4], o[5]),
+                   pack2_bf16(o[6], o[7]));
   }
 }
 

@@ -498,33 +498,34 @@ bool plan_attend_tc(int B, int H, int W, int C, int heads, int S, int topk, int 
   return false;
 }
 
-// The projection kernel: C a multiple of 64 up to 256. W stays resident in
-// shared memory when it fits (C <= 128); ring depths are the deepest that fit.
-bool plan_qkv(int M, int C, bra::QkvGeom *g, size_t *smem) {
-  if (C % 64 || C < 64 || C > 256 || M <= 0) return false;
+// The tcgen05 GEMM (qkv_tc.cuh): K and N multiples of 64 (N / 64 <= 12 for a
+// resident W), the output split into tensors of ow channels. W stays resident
+// in shared memory when it fits; ring depths are the deepest that fit.
+bool plan_linear(int M, int K, int N, int ow, bra::QkvGeom *g, size_t *smem) {
+  if (K % 64 || N % 64 || ow % 64 || N % ow || N / ow > 3 || K < 64 || M <= 0) return false;
   bra::QkvGeom a = {};
-  a.M = M; a.C = C;
-  a.ka = C / 64;
-  a.nt = 3 * C / 64;
+  a.M = M; a.K = K; a.N = N; a.ow = ow;
+  a.ka = K / 64;
+  a.nt = N / 64;
   a.tiles = (M + 127) / 128;
   const size_t x_stage = (size_t)a.ka * 16384, w_stage = (size_t)a.ka * 8192;
-  const size_t tail = round_up((size_t)3 * C * 4, 16) + bra::kQbCount * 8 + 16;
+  const size_t tail = round_up((size_t)N * 4, 16) + bra::kQbCount * 8 + 16;
   struct Cfg { int nx, nw, ns, res; };
   // staging tiles: one to three for each epilogue warpgroup
   constexpr int E = bra::kQkvEpi;
   const Cfg cfgs[] = {{4, a.nt, 3 * E, 1}, {3, a.nt, 3 * E, 1}, {2, a.nt, 3 * E, 1},
                       {2, a.nt, 2 * E, 1}, {2, a.nt, E, 1},     {2, 3, 2 * E, 0},
                       {2, 3, E, 0},        {2, 2, E, 0},        {1, 3, E, 0},
-                      {1, 2, E, 0}};
+                      {1, 2, E, 0},        {1, a.nt, E, 1},     {1, 1, E, 0}};
   for (const Cfg &c : cfgs) {
     if (c.res && a.nt > 12) continue;
     a.nx = c.nx; a.nw = c.nw; a.ns = c.ns; a.w_resident = c.res;
-    a.gw = c.res ? 3 : 1;
-    a.nacc = c.res ? 2 : 4;
+    a.gw = (c.res && a.nt % 3 == 0) ? 3 : 1;
+    a.nacc = a.gw == 3 ? 2 : 4;
     a.off_w = (uint32_t)(c.nx * x_stage);
     a.off_st = (uint32_t)(a.off_w + c.nw * w_stage);
     a.off_b = a.off_st + (uint32_t)c.ns * 16384u;
-    a.off_bar = (uint32_t)round_up(a.off_b + (size_t)3 * C * 4, 16);
+    a.off_bar = (uint32_t)round_up(a.off_b + (size_t)N * 4, 16);
     *smem = (size_t)a.off_st + (size_t)c.ns * 16384 + tail + 1024;
     if (*smem <= kMaxSmemPerBlock) {
       *g = a;
@@ -532,6 +533,29 @@ bool plan_qkv(int M, int C, bra::QkvGeom *g, size_t *smem) {
     }
   }
   return false;
+}
+
+// Enqueues the GEMM: outputs o[0..N/ow) of [M][ow] each, the residual (the
+// layout of the single output) added when given.
+int launch_linear(const void *x, const void *w, const float *bias, int M, int K, int N, int ow,
+                  void *const *o, const void *res, cudaStream_t s) {
+  bra::QkvGeom g;
+  size_t smem;
+  if (!plan_linear(M, K, N, ow, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+  CUtensorMap tx, tw;
+  if (!make_map_2d(&tx, x, M, K, 128) || !make_map_2d(&tw, w, N, K, 64)) return BRA_ERR_CUDA;
+  (void)cudaGetLastError();
+  auto kern = res ? bra::bra_qkv_tc_kernel<true> : bra::bra_qkv_tc_kernel<false>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  const unsigned grid = (unsigned)std::min(g.tiles, sm_count());
+  const int nout = N / ow;
+  kern<<<grid, bra::kQkvThreads, smem, s>>>(
+      tx, tw, bias, g, static_cast<__nv_bfloat16 *>(o[0]),
+      static_cast<__nv_bfloat16 *>(nout > 1 ? o[1] : o[0]),
+      static_cast<__nv_bfloat16 *>(nout > 2 ? o[2] : o[0]),
+      static_cast<const __nv_bfloat16 *>(res));
+  return cuda_status(cudaGetLastError());
 }
 
 // The image-resident kernel: bf16, regions of fewer than 16 tokens (a 16-row
@@ -1016,22 +1040,29 @@ int bra_qkv_project(const void *x, const void *w, const float *bias, long long M
     for (int j = 0; j < i; ++j)
       if (overlap(outs[i], bytes, outs[j], bytes)) return BRA_ERR_INVALID_ARG;
   }
+  if (dtype != BRA_BF16 || M > 0x7fffffffll - 127 || C > 256) return BRA_ERR_UNSUPPORTED;
+  void *qkv[3] = {q, k, v};
+  return launch_linear(x, w, bias, (int)M, C, 3 * C, C, qkv, nullptr,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int bra_linear(const void *x, const void *w, const float *bias, long long M, int K, int N,
+               const void *residual, int dtype, void *y, void *stream) {
+  if (M < 0 || K <= 0 || N <= 0) return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_F32 && dtype != BRA_BF16) return BRA_ERR_INVALID_ARG;
+  if (M == 0) return BRA_OK;
+  if (!x || !w || !y) return BRA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (residual && !aligned16(residual)))
+    return BRA_ERR_INVALID_ARG;
+  const size_t e = elem_size(dtype);
+  const size_t xb = (size_t)M * K * e, yb = (size_t)M * N * e;
+  if (overlap(y, yb, x, xb) || overlap(y, yb, w, (size_t)N * K * e) ||
+      (residual && residual != y && overlap(y, yb, residual, yb)))
+    return BRA_ERR_INVALID_ARG;
   if (dtype != BRA_BF16 || M > 0x7fffffffll - 127) return BRA_ERR_UNSUPPORTED;
-  bra::QkvGeom g;
-  size_t smem;
-  if (!plan_qkv((int)M, C, &g, &smem)) return BRA_ERR_UNSUPPORTED;
-  CUtensorMap tx, tw;
-  if (!make_map_2d(&tx, x, (int)M, C, 128) || !make_map_2d(&tw, w, 3 * C, C, 64))
-    return BRA_ERR_CUDA;
-  (void)cudaGetLastError();
-  auto kern = bra::bra_qkv_tc_kernel;
-  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
-    return BRA_ERR_CUDA;
-  const unsigned grid = (unsigned)std::min(g.tiles, sm_count());
-  kern<<<grid, bra::kQkvThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-      tx, tw, bias, g, static_cast<__nv_bfloat16 *>(q),
-      static_cast<__nv_bfloat16 *>(k), static_cast<__nv_bfloat16 *>(v));
-  return cuda_status(cudaGetLastError());
+  void *outs[1] = {y};
+  return launch_linear(x, w, bias, (int)M, K, N, N, outs, residual,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int bra_forward_launches(int B, int H, int W, int C, int heads, int S, int topk, int lepe_ks,
@@ -1087,6 +1118,64 @@ int bra_residual_add(const void *x, const void *r, long long n, int dtype, void 
       static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(r), n8,
       static_cast<__nv_bfloat16 *>(y));
   return cuda_status(cudaGetLastError());
+}
+
+int bra_dwconv_gelu(const void *h, const float *w, const float *bias, int B, int H, int W,
+                    int Ch, int dtype, void *y, void *stream) {
+  if (B < 0 || H <= 0 || W <= 0 || Ch <= 0) return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_F32 && dtype != BRA_BF16) return BRA_ERR_INVALID_ARG;
+  if (B == 0) return BRA_OK;
+  if (!h || !w || !y || !aligned16(h) || !aligned16(y)) return BRA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)B * H * W * Ch * elem_size(dtype);
+  if (overlap(h, bytes, y, bytes)) return BRA_ERR_INVALID_ARG;
+  // a block: all chunks of an 8-token tile row, Ch / 8 x 8 threads
+  if (dtype != BRA_BF16 || Ch % 8 || Ch / 8 * bra::kDwTile > bra::kDwMaxThreads)
+    return BRA_ERR_UNSUPPORTED;
+  const long long tiles = (long long)B * ((H + bra::kDwTile - 1) / bra::kDwTile) *
+                          ((W + bra::kDwTile - 1) / bra::kDwTile);
+  if (tiles > 0x7fffffffll) return BRA_ERR_UNSUPPORTED;
+  (void)cudaGetLastError();
+  auto kern = bra::bra_dwconv_gelu_kernel;
+  kern<<<(unsigned)tiles, (unsigned)(Ch / 8 * bra::kDwTile), 0,
+         static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16 *>(h), w, bias, B, H, W, Ch,
+      static_cast<__nv_bfloat16 *>(y));
+  return cuda_status(cudaGetLastError());
+}
+
+size_t bra_block_ffn_workspace_bytes(int B, int H, int W, int C) {
+  if (B < 0 || H <= 0 || W <= 0 || C <= 0) return 0;
+  // the normalised tokens [M][C], the hidden layer before and after the
+  // convolution and GELU [M][3C] each (bf16)
+  return (size_t)7 * B * H * W * C * 2;
+}
+
+int bra_block_ffn(const void *x, const float *ln_w, const float *ln_b, float eps, const void *w1,
+                  const float *b1, const float *conv_w, const float *conv_b, const void *w2,
+                  const float *b2, int B, int H, int W, int C, int dtype, void *workspace,
+                  void *y, void *stream) {
+  if (B < 0 || H <= 0 || W <= 0 || C <= 0 || !(eps >= 0.f)) return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_F32 && dtype != BRA_BF16) return BRA_ERR_INVALID_ARG;
+  if (B == 0) return BRA_OK;
+  if (!x || !w1 || !conv_w || !w2 || !workspace || !y) return BRA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(workspace) || !aligned16(y)) return BRA_ERR_INVALID_ARG;
+  const size_t mc = (size_t)B * H * W * C;
+  const size_t bytes = mc * elem_size(dtype);
+  const size_t ws = bra_block_ffn_workspace_bytes(B, H, W, C);
+  if (overlap(y, bytes, x, bytes) || overlap(y, bytes, workspace, ws) ||
+      overlap(x, bytes, workspace, ws))
+    return BRA_ERR_INVALID_ARG;
+  if (dtype != BRA_BF16) return BRA_ERR_UNSUPPORTED;
+  uint8_t *w8 = static_cast<uint8_t *>(workspace);
+  void *xn = w8, *hid = w8 + 2 * mc, *act = w8 + 8 * mc;
+  const long long M = (long long)B * H * W;
+  int rc = bra_layer_norm(x, ln_w, ln_b, M, C, eps, dtype, xn, stream);
+  if (rc) return rc;
+  rc = bra_linear(xn, w1, b1, M, C, 3 * C, nullptr, dtype, hid, stream);
+  if (rc) return rc;
+  rc = bra_dwconv_gelu(hid, conv_w, conv_b, B, H, W, 3 * C, dtype, act, stream);
+  if (rc) return rc;
+  return bra_linear(act, w2, b2, M, 3 * C, C, x, dtype, y, stream);
 }
 
 size_t bra_block_attention_workspace_bytes(int B, int H, int W, int C, int S, int topk) {

@@ -40,15 +40,17 @@ constexpr int kQkvThreads = 128 + 128 * kQkvEpi;
 constexpr uint32_t kQkvTmemCols = 512;
 
 struct QkvGeom {
-  int M, C;
-  int ka;           // 64-channel atoms along K, C / 64
-  int nt;           // 64-channel output tiles, 3C / 64
+  int M, K, N;      // x [M][K], W [N][K]; outputs N channels in all
+  int ow;           // channels of each output tensor (N: one tensor; N / 3: q, k, v)
+  int ka;           // 64-channel atoms along K, K / 64
+  int nt;           // 64-channel output tiles, N / 64
   int tiles;        // 128-token tiles
   int nx, nw, ns;   // x ring (<= 4), weight ring (<= 12), staging tiles (1 to 3 for
                     // each epilogue warpgroup)
   int w_resident;   // the whole W stays in shared memory (nw == nt), stored atom-major
                     // ([ka][nt][64 rows]) so that 3 output tiles form one N = 192 operand
-  int gw;           // output tiles per MMA group: 3 (N = 192) with W resident, else 1
+  int gw;           // output tiles per MMA group: 3 (N = 192) with W resident and nt a
+                    // multiple of 3, else 1
   int nacc;         // tensor-memory accumulators: 2 of 256 columns (gw 3) or 4 of 64
   uint32_t off_w, off_st, off_b, off_bar;  // x ring at 0
 };
@@ -77,15 +79,17 @@ __device__ __forceinline__ void qkv_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// RES: a residual of the output's layout is added before the rounding.
+template <bool RES>
 __global__ void __launch_bounds__(kQkvThreads, 1)
     bra_qkv_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_w,
                       const float *__restrict__ bias, QkvGeom g,
                       __nv_bfloat16 *__restrict__ oq, __nv_bfloat16 *__restrict__ ok,
-                      __nv_bfloat16 *__restrict__ ov) {
+                      __nv_bfloat16 *__restrict__ ov, const __nv_bfloat16 *__restrict__ res) {
   extern __shared__ uint8_t qkv_smem_raw[];
   uint8_t *smem = qkv_smem_raw + ((1024u - (smem_u32(qkv_smem_raw) & 1023u)) & 1023u);
-  float *sb = reinterpret_cast<float *>(smem + g.off_b);  // [3C]
+  float *sb = reinterpret_cast<float *>(smem + g.off_b);  // [N]
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + g.off_bar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kQbCount);
 
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
     mbar_init(&bars[kQbDone], 1);
     fence_mbar_init();
   }
-  for (int e = tid; e < 3 * g.C; e += kQkvThreads) sb[e] = bias ? __ldg(bias + e) : 0.f;
+  for (int e = tid; e < g.N; e += kQkvThreads) sb[e] = bias ? __ldg(bias + e) : 0.f;
   if (warp == 1) {
     tmem_alloc(tmem_slot, kQkvTmemCols);
     tmem_relinquish();
@@ -223,16 +227,30 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
         __syncwarp();
         uint8_t *row = smem + g.off_st + ss * 16384 + r * 128;
         const float *bn = sb + n * 64;
+        const int otiles = g.ow / 64;
+        const int t = n / otiles, cc = n % otiles;  // output tensor; its 64-channel chunk
+        const long long mr = 128ll * tile + r;       // this thread's token
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: output channels 8c .. 8c+7
           const uint32_t *src = c < 4 ? v0 + 8 * c : v1 + 8 * (c - 4);
           const float4 b0 = *reinterpret_cast<const float4 *>(bn + 8 * c);
           const float4 b1 = *reinterpret_cast<const float4 *>(bn + 8 * c + 4);
-          const uint4 packed = make_uint4(
-              pack_bf16x2(__uint_as_float(src[0]) + b0.x, __uint_as_float(src[1]) + b0.y),
-              pack_bf16x2(__uint_as_float(src[2]) + b0.z, __uint_as_float(src[3]) + b0.w),
-              pack_bf16x2(__uint_as_float(src[4]) + b1.x, __uint_as_float(src[5]) + b1.y),
-              pack_bf16x2(__uint_as_float(src[6]) + b1.z, __uint_as_float(src[7]) + b1.w));
+          float f[8] = {__uint_as_float(src[0]) + b0.x, __uint_as_float(src[1]) + b0.y,
+                        __uint_as_float(src[2]) + b0.z, __uint_as_float(src[3]) + b0.w,
+                        __uint_as_float(src[4]) + b1.x, __uint_as_float(src[5]) + b1.y,
+                        __uint_as_float(src[6]) + b1.z, __uint_as_float(src[7]) + b1.w};
+          if (RES && mr < g.M) {  // the residual, added before the one rounding
+            const uint4 rv = __ldg(reinterpret_cast<const uint4 *>(
+                res + mr * g.ow + 64 * cc + 8 * c));
+            const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              f[2 * e] += __uint_as_float(rw[e] << 16);
+              f[2 * e + 1] += __uint_as_float(rw[e] & 0xffff0000u);
+            }
+          }
+          const uint4 packed = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                          pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
           *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = packed;
         }
         __syncwarp();
@@ -240,7 +258,6 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
         // unit is left to the x loads): 4 whole rows, 512 contiguous bytes,
         // per instruction
         {
-          const int t = n / g.ka, cc = n % g.ka;  // q, k or v; channel chunk
           __nv_bfloat16 *dst = t == 0 ? oq : (t == 1 ? ok : ov);
           const uint8_t *tile_st = smem + g.off_st + ss * 16384;
           const int w4 = warp & 3, ch = lane & 7;
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
             const long long m = 128ll * tile + rr;
             const uint4 val =
                 *reinterpret_cast<const uint4 *>(tile_st + rr * 128 + ((ch ^ (rr & 7)) << 4));
-            if (m < g.M) *reinterpret_cast<uint4 *>(dst + m * g.C + 64 * cc + 8 * ch) = val;
+            if (m < g.M) *reinterpret_cast<uint4 *>(dst + m * g.ow + 64 * cc + 8 * ch) = val;
           }
         }
         }
