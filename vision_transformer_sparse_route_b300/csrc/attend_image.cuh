@@ -41,6 +41,7 @@ struct ImageGeom {
   uint32_t tile;     // bytes of one [H*W + 1][128 B] tile (the last row stays
                      // zero), rounded to 1024
   uint32_t off_k, off_v, off_h, off_o, off_w, off_tab, off_bar;
+  uint32_t off_rt;   // local form: region and token offset tables
   float scale_log2;  // d^-1/2 * log2(e)
 };
 
@@ -163,37 +164,39 @@ __device__ __forceinline__ void image_attention_task(const ImageGeom &g, int i, 
 }
 
 // The same attention in transposed form, for regions of at most 8 tokens,
-// both heads of the chunk at once (two independent MMA chains for the warp;
-// the key table lookups and token addresses are shared): the keys are the
+// NH heads of the chunk from head h0 on at once (NH = 2: two independent MMA
+// chains for the warp, sharing the key table lookups and token addresses;
+// NH = 1 keeps the registers under 64): the keys are the
 // MMA's 16 rows and the region's queries its 8 columns, so that half of each
 // MMA carries a query instead of a quarter. S^T = K Q^T; the softmax runs
 // down each column (a lane holds 8 of a column's 64 keys, three shuffles
 // combine them); movmatrix turns each 8x8 block of the bf16 P^T into the B
 // operand of O^T = V^T P^T; the column sums are an MMA of ones against the
-// same bf16 P^T. Leaves O^T of head h (channels h*32 + ct*16 + lane/4 and +8,
-// queries 2*(lane%4) and +1) in ot[h][ct][0..3] = (ch, q0), (ch, q1),
-// (ch+8, q0), (ch+8, q1).
-template <bool MASKED>
+// same bf16 P^T. Leaves O^T of head h0 + h (channels (h0+h)*32 + ct*16 +
+// lane/4 and +8, queries 2*(lane%4) and +1) in ot[h][ct][0..3] = (ch, q0),
+// (ch, q1), (ch+8, q0), (ch+8, q1).
+template <bool MASKED, int NH = 2>
 __device__ __forceinline__ void image_attention_region_t(const ImageGeom &g, int i,
                                                          uint32_t q_base, uint32_t k_base,
                                                          uint32_t v_base, const uint16_t *kt,
-                                                         float (&ot)[2][2][4], int lane) {
+                                                         float (&ot)[NH][2][4], int lane,
+                                                         int h0 = 0) {
   const int y0 = (i / g.S) * g.hr, x0 = (i % g.S) * g.wr;
   // Q^T as the B operand: one 8x8 block (queries x 8 channels) per chunk
-  uint32_t qb[2][2][2];
+  uint32_t qb[NH][2][2];
   {
     int r = lane & 7;
     r = r < g.n ? r : 0;  // columns past the region repeat its first token
     const int tok = (y0 + r / g.wr) * g.W + x0 + r % g.wr;
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-      ldsm_x4(q_base + tok_addr(tok, h * 4 + (lane >> 3)), qb[h][0][0], qb[h][0][1],
+    for (int h = 0; h < NH; ++h)
+      ldsm_x4(q_base + tok_addr(tok, (h0 + h) * 4 + (lane >> 3)), qb[h][0][0], qb[h][0][1],
               qb[h][1][0], qb[h][1][1]);
   }
-  float l4[2][4];
-  float m_run[2][2];
+  float l4[NH][4];
+  float m_run[NH][2];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     m_run[h][0] = m_run[h][1] = -INFINITY;  // columns 2*(lane%4) and +1
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -208,33 +211,33 @@ __device__ __forceinline__ void image_attention_region_t(const ImageGeom &g, int
   const int vr = (lane & 7) + (lane >> 4) * 8;        // V block row of this lane
 
   for (int kb = 0; kb < g.nkeys; kb += 64) {
-    float s[2][4][4];
+    float s[NH][4][4];
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
       const int tok = kt[kb + mt * 16 + kr];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NH; ++h) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[h][mt][e] = 0.f;
         uint32_t a[4];
-        ldsm_x4(k_base + tok_addr(tok, h * 4 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        ldsm_x4(k_base + tok_addr(tok, (h0 + h) * 4 + (lane >> 4)), a[0], a[1], a[2], a[3]);
         mma_bf16_16816(s[h][mt], a, qb[h][0][0], qb[h][0][1]);
-        ldsm_x4(k_base + tok_addr(tok, h * 4 + 2 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        ldsm_x4(k_base + tok_addr(tok, (h0 + h) * 4 + 2 + (lane >> 4)), a[0], a[1], a[2], a[3]);
         mma_bf16_16816(s[h][mt], a, qb[h][1][0], qb[h][1][1]);
       }
     }
     if (MASKED) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < NH; ++h)
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (kb + mt * 16 + (lane >> 2) + (e >> 1) * 8 >= g.nkeys) s[h][mt][e] = -INFINITY;
     }
-    float2 nb[2];
+    float2 nb[NH];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       float m0 = max3(s[h][0][0], s[h][0][2], s[h][1][0]);
       m0 = max3(m0, s[h][1][2], s[h][2][0]);
       m0 = max3(m0, s[h][2][2], s[h][3][0]);
@@ -271,7 +274,7 @@ __device__ __forceinline__ void image_attention_region_t(const ImageGeom &g, int
     for (int mt = 0; mt < 4; ++mt) {
       const int tok = kt[kb + mt * 16 + vr];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NH; ++h) {
         // bf16 P^T rows g (keys mt*16 + g) and g + 8, columns q0, q1;
         // transposed into the B fragments of keys 0-7 and 8-15 of this block
         const float2 xt = __ffma2_rn(make_float2(s[h][mt][0], s[h][mt][1]), sc2, nb[h]);
@@ -281,8 +284,8 @@ __device__ __forceinline__ void image_attention_region_t(const ImageGeom &g, int
 #pragma unroll
         for (int ct = 0; ct < 2; ++ct) {
           uint32_t a[4];
-          ldsm_x4_trans(v_base + tok_addr(tok, h * 4 + ct * 2 + ((lane >> 3) & 1)), a[0], a[1],
-                        a[2], a[3]);
+          ldsm_x4_trans(v_base + tok_addr(tok, (h0 + h) * 4 + ct * 2 + ((lane >> 3) & 1)), a[0],
+                        a[1], a[2], a[3]);
           mma_bf16_16816(ot[h][ct], a, pb0, pb1);
         }
         mma_bf16_16816(l4[h], ones, pb0, pb1);  // column sums of the bf16 P^T
@@ -290,7 +293,7 @@ __device__ __forceinline__ void image_attention_region_t(const ImageGeom &g, int
     }
   }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     const float inv0 = 1.f / l4[h][0], inv1 = 1.f / l4[h][1];
 #pragma unroll
     for (int ct = 0; ct < 2; ++ct) {
@@ -344,6 +347,84 @@ __device__ __forceinline__ void image_lepe_item(const ImageGeom &g, const uint8_
   }
 }
 
+// The common start of the image kernels after thread 0 has issued the tile
+// copies, all threads: stage the chunk's LePE weights (tap-major, bias after
+// them) and build the key table from the routing (the previous grid's
+// output): keys m*n .. m*n+n-1 of query region i are the tokens of routed
+// region idx[b, i, m] in row-major order, as image token numbers in ktab and,
+// when vtab is given, as positions in the V halo tile (image plus a border of
+// ks/2, halo_w wide) in vtab. An out-of-range region's keys and the keys past
+// nkeys (masked) name the zero row after the image's tokens (the zero row
+// after the halo in vtab).
+template <int KS, int NT = kImgThreads>
+__device__ __forceinline__ void image_tables(const ImageGeom &g, float *sw, uint16_t *ktab,
+                                             uint16_t *vtab, const int32_t *__restrict__ idx,
+                                             const float *__restrict__ lepe_w,
+                                             const float *__restrict__ lepe_b, int b, int cc,
+                                             int tid) {
+  constexpr int PAD = KS / 2;
+  // this chunk's LePE weights, read in their [c][tap] order (every load
+  // issued before the first store), stored tap-major
+  constexpr int NW = (64 * KS * KS + NT - 1) / NT;
+  float wv[NW];
+#pragma unroll
+  for (int u = 0; u < NW; ++u) {
+    const int e = tid + u * NT;
+    wv[u] = e < 64 * KS * KS ? __ldg(lepe_w + (size_t)cc * 64 * KS * KS + e) : 0.f;
+  }
+  const float bv = (tid < 64 && lepe_b) ? __ldg(lepe_b + cc * 64 + tid) : 0.f;
+  grid_dependency_wait();  // the routing comes from the previous grid
+  // the thread's first routing entries (up to four), loaded together before
+  // the weights are stored so that all these loads overlap
+  const int slots = g.R * g.topk;
+  int jpre[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    jpre[u] = tid + u * NT < slots ? __ldg(idx + (size_t)b * slots + tid + u * NT) : 0;
+#pragma unroll
+  for (int u = 0; u < NW; ++u) {
+    const int e = tid + u * NT;
+    if (e < 64 * KS * KS) {
+      const int c = e / (KS * KS), tap = e - c * (KS * KS);
+      sw[tap * 64 + c] = wv[u];
+    }
+  }
+  if (tid < 64) sw[KS * KS * 64 + tid] = bv;
+  const uint16_t zero_row = static_cast<uint16_t>(g.H * g.W);
+  const uint16_t zero_pos = static_cast<uint16_t>(g.halo_w * g.halo_h);
+  for (int e = tid, u = 0; e < slots; e += NT, ++u) {
+    const int i = e / g.topk, m = e - i * g.topk;
+    int j = jpre[0];
+#pragma unroll
+    for (int v = 1; v < 4; ++v) j = u == v ? jpre[v] : j;
+    if (u >= 4) j = __ldg(idx + (size_t)b * slots + e);
+    uint16_t *row = ktab + i * g.nkp + m * g.n;
+    uint16_t *vrow = vtab ? vtab + i * g.nkp + m * g.n : nullptr;
+    if (j < 0 || j >= g.R) {  // out of range: flag it
+      atomicOr(&g_status, kStatusBadIndex);
+      for (int t = 0; t < g.n; ++t) {
+        row[t] = zero_row;
+        if (vrow) vrow[t] = zero_pos;
+      }
+    } else {
+      const int y0 = (j / g.S) * g.hr, x0 = (j % g.S) * g.wr;
+      for (int ty = 0; ty < g.hr; ++ty)
+        for (int tx = 0; tx < g.wr; ++tx) {
+          row[ty * g.wr + tx] = static_cast<uint16_t>((y0 + ty) * g.W + x0 + tx);
+          if (vrow)
+            vrow[ty * g.wr + tx] =
+                static_cast<uint16_t>((y0 + ty + PAD) * g.halo_w + x0 + tx + PAD);
+        }
+    }
+  }
+  const int tail = g.nkp - g.nkeys;
+  for (int e = tid; e < g.R * tail; e += NT) {
+    const int i = e / tail, key = g.nkeys + (e - i * tail);
+    ktab[i * g.nkp + key] = zero_row;
+    if (vtab) vtab[i * g.nkp + key] = zero_pos;
+  }
+}
+
 template <int KS, int RB>
 __global__ void __launch_bounds__(kImgThreads, 1)
     bra_attend_image_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -365,7 +446,6 @@ __global__ void __launch_bounds__(kImgThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / g.nc, cc = blockIdx.x % g.nc;
   constexpr int PAD = KS / 2;
-
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
@@ -375,58 +455,11 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     tma_load_4d(smem + g.off_v, &tm_v, bar, cc * 64, 0, 0, b);
     tma_load_4d(smem + g.off_h, &tm_vh, bar, cc * 64, -PAD, -PAD, b);
   }
-  // this chunk's LePE weights, read in their [c][tap] order (every load
-  // issued before the first store), stored tap-major
-  constexpr int NW = (64 * KS * KS + kImgThreads - 1) / kImgThreads;
-  float wv[NW];
-#pragma unroll
-  for (int u = 0; u < NW; ++u) {
-    const int e = tid + u * kImgThreads;
-    wv[u] = e < 64 * KS * KS ? __ldg(lepe_w + (size_t)cc * 64 * KS * KS + e) : 0.f;
-  }
-  const float bv = (tid < 64 && lepe_b) ? __ldg(lepe_b + cc * 64 + tid) : 0.f;
-  // the first routing entry of this thread (it comes from the previous grid),
-  // loaded before the weights are stored so that the two loads overlap
-  grid_dependency_wait();
-  const int slots = g.R * g.topk;
-  const int j0 = tid < slots ? __ldg(idx + (size_t)b * slots + tid) : 0;
-#pragma unroll
-  for (int u = 0; u < NW; ++u) {
-    const int e = tid + u * kImgThreads;
-    if (e < 64 * KS * KS) {
-      const int c = e / (KS * KS), tap = e - c * (KS * KS);
-      sw[tap * 64 + c] = wv[u];
-    }
-  }
-  if (tid < 64) sw[KS * KS * 64 + tid] = bv;
   // the zero row of K and V (no copy writes it)
   if (tid < 16)
     *reinterpret_cast<uint4 *>(smem + (tid < 8 ? g.off_k : g.off_v) + g.H * g.W * 128 +
                                (tid & 7) * 16) = make_uint4(0, 0, 0, 0);
-  // The key table, one (query region i, routed slot m) at a time: keys
-  // m*n .. m*n+n-1 of region i are the tokens of routed region idx[b, i, m]
-  // in row-major order. An out-of-range region's keys and the keys past nkeys
-  // (masked) read the zero row after the image's tokens.
-  const uint16_t zero_row = static_cast<uint16_t>(g.H * g.W);
-  for (int e = tid; e < slots; e += kImgThreads) {
-    const int i = e / g.topk, m = e - i * g.topk;
-    const int j = e == tid ? j0 : __ldg(idx + (size_t)b * slots + e);
-    uint16_t *row = ktab + i * g.nkp + m * g.n;
-    if (j < 0 || j >= g.R) {  // out of range: flag it
-      atomicOr(&g_status, kStatusBadIndex);
-      for (int t = 0; t < g.n; ++t) row[t] = zero_row;
-    } else {
-      const int y0 = (j / g.S) * g.hr, x0 = (j % g.S) * g.wr;
-      for (int ty = 0; ty < g.hr; ++ty)
-        for (int tx = 0; tx < g.wr; ++tx)
-          row[ty * g.wr + tx] = static_cast<uint16_t>((y0 + ty) * g.W + x0 + tx);
-    }
-  }
-  const int tail = g.nkp - g.nkeys;
-  for (int e = tid; e < g.R * tail; e += kImgThreads) {
-    const int i = e / tail;
-    ktab[i * g.nkp + g.nkeys + (e - i * tail)] = zero_row;
-  }
+  image_tables<KS>(g, sw, ktab, nullptr, idx, lepe_w, lepe_b, b, cc, tid);
   __syncthreads();
   mbar_wait(bar, 0);
 
@@ -496,6 +529,324 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     const int cp = item % 32, rest = item / 32;
     const int x = rest % g.W, ry0 = (rest / g.W) * RB;
     image_lepe_item<KS, RB>(g, hb, so, gout, 2 * cp, x, ry0, sw);
+  }
+  if (tid == 0) settle_after_timeout();
+}
+
+// ---- the local form, regions of at most 8 tokens: about half the shared
+// memory of the form above, so that two CTAs share an SM. K is the swizzled
+// tile as above; V is a zero-bordered halo tile (image plus ks/2 on every
+// side) with 144-byte rows (the 64 channels of the chunk and 16 unused
+// bytes; the odd 16-byte pitch keeps ldmatrix free of bank conflicts as the
+// swizzle does); Q is read by each task from global memory straight into its
+// MMA fragment, and there is no f32 O tile. Each warp runs (query region,
+// head) tasks; after a task's attention the warp computes the LePE of the
+// region's tokens over the head's 32 channels from the halo tile, adds the
+// task's O and stores bf16.
+
+constexpr int kStgStride = 68;  // floats a staged O row (64 channels + pad)
+constexpr int kLocalWarps = 8;
+constexpr int kLocalThreads = 32 * kLocalWarps;
+constexpr int kHaloPitch = 144;  // bytes a V halo row
+
+// O^T of a region's NH heads from head h0 on (t0: the region's first image
+// token, toff: each token's offset from it), as image_attention_region_t,
+// with Q taken from global memory (qg: the image's first token at the
+// chunk's first channel) and V from the halo tile through the halo-position
+// key table vt.
+template <bool MASKED, int NH>
+__device__ __forceinline__ void local_attention(const ImageGeom &g, int t0, const uint16_t *toff,
+                                                int h0, const __nv_bfloat16 *qg,
+                                                uint32_t k_base, uint32_t vh_base,
+                                                const uint16_t *kt, const uint16_t *vt,
+                                                float (&ot)[NH][2][4], int lane) {
+  // Q^T as the B operand: lane holds query lane/4 (queries past the region
+  // repeat its first token), channels kb*16 + 2*(lane%4) + {0, 1} and + 8
+  uint32_t qb[NH][2][2];
+  {
+    const int r = lane >> 2;
+    const int tok = t0 + (r < g.n ? toff[r] : 0);
+    const uint32_t *qp = reinterpret_cast<const uint32_t *>(qg + (size_t)tok * g.C) +
+                         (lane & 3);
+#pragma unroll
+    for (int h = 0; h < NH; ++h)
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+        qb[h][kb][0] = __ldg(qp + (h0 + h) * 16 + kb * 8);
+        qb[h][kb][1] = __ldg(qp + (h0 + h) * 16 + kb * 8 + 4);
+      }
+  }
+  float l4[NH][4], m_run[NH][2];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    m_run[h][0] = m_run[h][1] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      l4[h][e] = 0.f;
+      ot[h][0][e] = 0.f;
+      ot[h][1][e] = 0.f;
+    }
+  }
+  const uint32_t ones[4] = {0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u};
+  const float2 sc2 = make_float2(g.scale_log2, g.scale_log2);
+  const int kr = (lane & 7) + ((lane >> 3) & 1) * 8;  // K block row of this lane
+  const int vr = (lane & 7) + (lane >> 4) * 8;        // V block row of this lane
+  for (int kb = 0; kb < g.nkeys; kb += 64) {
+    float s[NH][4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int tok = kt[kb + mt * 16 + kr];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[h][mt][e] = 0.f;
+        uint32_t a[4];
+        ldsm_x4(k_base + tok_addr(tok, (h0 + h) * 4 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(s[h][mt], a, qb[h][0][0], qb[h][0][1]);
+        ldsm_x4(k_base + tok_addr(tok, (h0 + h) * 4 + 2 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(s[h][mt], a, qb[h][1][0], qb[h][1][1]);
+      }
+    }
+    if (MASKED) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (kb + mt * 16 + (lane >> 2) + (e >> 1) * 8 >= g.nkeys) s[h][mt][e] = -INFINITY;
+    }
+    float2 nb[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      float m0 = max3(s[h][0][0], s[h][0][2], s[h][1][0]);
+      m0 = max3(m0, s[h][1][2], s[h][2][0]);
+      m0 = max3(m0, s[h][2][2], s[h][3][0]);
+      m0 = fmaxf(m0, s[h][3][2]);
+      float m1 = max3(s[h][0][1], s[h][0][3], s[h][1][1]);
+      m1 = max3(m1, s[h][1][3], s[h][2][1]);
+      m1 = max3(m1, s[h][2][3], s[h][3][1]);
+      m1 = fmaxf(m1, s[h][3][3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+      }
+      const float mx[2] = {m0, m1};
+      float base[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float m_new = fmaxf(m_run[h][q], mx[q] * g.scale_log2);
+        base[q] = (m_new == -INFINITY) ? 0.f : m_new;
+        if (kb > 0) {
+          const float alpha = exp2f(m_run[h][q] - base[q]);
+          ot[h][0][q] *= alpha;
+          ot[h][0][q + 2] *= alpha;
+          ot[h][1][q] *= alpha;
+          ot[h][1][q + 2] *= alpha;
+          l4[h][q] *= alpha;
+          l4[h][q + 2] *= alpha;
+        }
+        m_run[h][q] = m_new;
+      }
+      nb[h] = make_float2(-base[0], -base[1]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const uint32_t vrow = vh_base + vt[kb + mt * 16 + vr] * kHaloPitch;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float2 xt = __ffma2_rn(make_float2(s[h][mt][0], s[h][mt][1]), sc2, nb[h]);
+        const float2 xb = __ffma2_rn(make_float2(s[h][mt][2], s[h][mt][3]), sc2, nb[h]);
+        const uint32_t pb0 = movmatrix_trans(exp2_bf16x2(xt.x, xt.y));
+        const uint32_t pb1 = movmatrix_trans(exp2_bf16x2(xb.x, xb.y));
+#pragma unroll
+        for (int ct = 0; ct < 2; ++ct) {
+          uint32_t a[4];
+          ldsm_x4_trans(vrow + ((h0 + h) * 4 + ct * 2 + ((lane >> 3) & 1)) * 16, a[0], a[1],
+                        a[2], a[3]);
+          mma_bf16_16816(ot[h][ct], a, pb0, pb1);
+        }
+        mma_bf16_16816(l4[h], ones, pb0, pb1);  // column sums of the bf16 P^T
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const float inv0 = 1.f / l4[h][0], inv1 = 1.f / l4[h][1];
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) {
+      ot[h][ct][0] *= inv0; ot[h][ct][1] *= inv1;
+      ot[h][ct][2] *= inv0; ot[h][ct][3] *= inv1;
+    }
+  }
+}
+
+// LePE + O of a region over the chunk's 64 channels: t0 and h0 are the
+// region's first image token and the halo position of that token's top-left
+// tap, toff and hoff each token's offset from them; ot is the region's O^T
+// fragment (both heads), stg the warp's staging rows ([n][kStgStride] f32),
+// vh the halo tile, sw the chunk's weights (tap-major, bias after them),
+// gout the image's first token at the chunk's first channel. Lane l takes
+// channels 2l, 2l+1 of every token of the region, its 25 weights in
+// registers and one 4-byte load of V a tap (the warp reads 128 contiguous
+// bytes). Each output is bias, then the taps in row-major order, then O,
+// rounded once; the halo's zero border stands for the padding. With the
+// region's shape HR x WR fixed at compile time the lane slides over the
+// region's window ((HR + KS - 1) x (WR + KS - 1) loads, each feeding every
+// output whose kernel covers it, in the same tap order); with HR = 0 it takes
+// the tokens one by one.
+template <int KS, int HR, int WR>
+__device__ __forceinline__ void local_lepe(const ImageGeom &g, int t0, int h0,
+                                           const uint16_t *toff, const uint16_t *hoff,
+                                           const float (&ot)[2][2][4], float *stg,
+                                           const uint8_t *vh, const float *sw,
+                                           __nv_bfloat16 *gout, int lane) {
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int q = 2 * (lane & 3) + e;
+    if (q < g.n) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            stg[q * kStgStride + h * 32 + ct * 16 + half * 8 + (lane >> 2)] =
+                ot[h][ct][2 * half + e];
+    }
+  }
+  const int c = 2 * lane;
+  float2 wgt[KS * KS];
+#pragma unroll
+  for (int e = 0; e < KS * KS; ++e) wgt[e] = *reinterpret_cast<const float2 *>(sw + e * 64 + c);
+  const float2 bias = *reinterpret_cast<const float2 *>(sw + KS * KS * 64 + c);
+  const uint32_t row_bytes = g.halo_w * kHaloPitch;
+  __syncwarp();
+  if constexpr (HR > 0) {
+    float2 acc[HR][WR];
+#pragma unroll
+    for (int ty = 0; ty < HR; ++ty)
+#pragma unroll
+      for (int tx = 0; tx < WR; ++tx) acc[ty][tx] = bias;
+    const uint8_t *tap0 = vh + h0 * kHaloPitch + 2 * c;
+#pragma unroll
+    for (int yy = 0; yy < HR + KS - 1; ++yy) {
+      const uint8_t *row = tap0 + yy * row_bytes;
+#pragma unroll
+      for (int xx = 0; xx < WR + KS - 1; ++xx) {
+        const uint32_t t2 = *reinterpret_cast<const uint32_t *>(row + xx * kHaloPitch);
+        const float2 v =
+            make_float2(__uint_as_float(t2 << 16), __uint_as_float(t2 & 0xffff0000u));
+#pragma unroll
+        for (int ty = 0; ty < HR; ++ty)
+#pragma unroll
+          for (int tx = 0; tx < WR; ++tx) {
+            const int u = yy - ty, w = xx - tx;
+            if (u >= 0 && u < KS && w >= 0 && w < KS)
+              acc[ty][tx] = __ffma2_rn(wgt[u * KS + w], v, acc[ty][tx]);
+          }
+      }
+    }
+#pragma unroll
+    for (int ty = 0; ty < HR; ++ty)
+#pragma unroll
+      for (int tx = 0; tx < WR; ++tx) {
+        const float2 ov =
+            *reinterpret_cast<const float2 *>(stg + (ty * WR + tx) * kStgStride + c);
+        const float2 sum = __fadd2_rn(acc[ty][tx], ov);
+        *reinterpret_cast<uint32_t *>(gout + (size_t)(t0 + ty * g.W + tx) * g.C + c) =
+            pack_bf16x2(sum.x, sum.y);
+      }
+  } else {
+    for (int r = 0; r < g.n; ++r) {
+      const uint8_t *tap0 = vh + (h0 + hoff[r]) * kHaloPitch + 2 * c;
+      float2 acc = bias;
+#pragma unroll
+      for (int u = 0; u < KS; ++u) {
+        const uint8_t *row = tap0 + u * row_bytes;
+#pragma unroll
+        for (int w = 0; w < KS; ++w) {
+          const uint32_t t2 = *reinterpret_cast<const uint32_t *>(row + w * kHaloPitch);
+          acc = __ffma2_rn(
+              wgt[u * KS + w],
+              make_float2(__uint_as_float(t2 << 16), __uint_as_float(t2 & 0xffff0000u)), acc);
+        }
+      }
+      const float2 ov = *reinterpret_cast<const float2 *>(stg + r * kStgStride + c);
+      const float2 sum = __fadd2_rn(acc, ov);
+      *reinterpret_cast<uint32_t *>(gout + (size_t)(t0 + toff[r]) * g.C + c) =
+          pack_bf16x2(sum.x, sum.y);
+    }
+  }
+  __syncwarp();
+}
+
+template <int KS, int HR, int WR>
+__global__ void __launch_bounds__(kLocalThreads, 2)
+    bra_attend_image_local_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                  const __grid_constant__ CUtensorMap tm_vh,
+                                  const __nv_bfloat16 *__restrict__ q,
+                                  __nv_bfloat16 *__restrict__ out,
+                                  const int32_t *__restrict__ idx,
+                                  const float *__restrict__ lepe_w,
+                                  const float *__restrict__ lepe_b, ImageGeom g) {
+  extern __shared__ uint8_t image_smem_raw[];
+  uint8_t *smem = image_smem_raw + ((1024u - (smem_u32(image_smem_raw) & 1023u)) & 1023u);
+  float *sw = reinterpret_cast<float *>(smem + g.off_w);
+  uint16_t *ktab = reinterpret_cast<uint16_t *>(smem + g.off_tab);
+  uint16_t *vtab = reinterpret_cast<uint16_t *>(smem + g.off_v);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + g.off_bar);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x / g.nc, cc = blockIdx.x % g.nc;
+  constexpr int PAD = KS / 2;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, g.H * g.W * 128 + g.halo_w * g.halo_h * kHaloPitch);
+    tma_load_4d(smem + g.off_k, &tm_k, bar, cc * 64, 0, 0, b);
+    tma_load_4d(smem + g.off_h, &tm_vh, bar, cc * 64, -PAD, -PAD, b);
+  }
+  // the zero rows after the K tile and after the halo (no copy writes them)
+  if (tid < 8)
+    *reinterpret_cast<uint4 *>(smem + g.off_k + g.H * g.W * 128 + tid * 16) =
+        make_uint4(0, 0, 0, 0);
+  else if (tid < 17)
+    *reinterpret_cast<uint4 *>(smem + g.off_h + g.halo_w * g.halo_h * kHaloPitch +
+                               (tid - 8) * 16) = make_uint4(0, 0, 0, 0);
+  image_tables<KS, kLocalThreads>(g, sw, ktab, vtab, idx, lepe_w, lepe_b, b, cc, tid);
+  // region tables: first image token and the halo position of its top-left
+  // tap ([R][2]); token offsets within a region, image and halo ([n][2])
+  uint16_t *rt = reinterpret_cast<uint16_t *>(smem + g.off_rt);
+  uint16_t *ot_tab = rt + 2 * g.R;
+  for (int e = tid; e < g.R + g.n; e += kLocalThreads) {
+    if (e < g.R) {
+      const int y0 = (e / g.S) * g.hr, x0 = (e % g.S) * g.wr;
+      rt[2 * e] = static_cast<uint16_t>(y0 * g.W + x0);
+      rt[2 * e + 1] = static_cast<uint16_t>(y0 * g.halo_w + x0);
+    } else {
+      const int r = e - g.R, dy = r / g.wr, dx = r % g.wr;
+      ot_tab[r] = static_cast<uint16_t>(dy * g.W + dx);
+      ot_tab[8 + r] = static_cast<uint16_t>(dy * g.halo_w + dx);
+    }
+  }
+  __syncthreads();
+  mbar_wait(bar, 0);
+
+  const uint32_t k_base = smem_u32(smem + g.off_k), vh_base = smem_u32(smem + g.off_h);
+  float *stg = reinterpret_cast<float *>(smem + g.off_o) + warp * g.n * kStgStride;
+  const size_t img = (size_t)b * g.H * g.W * g.C + cc * 64;
+  for (int i = warp; i < g.R; i += kLocalWarps) {
+    const int t0 = rt[2 * i], h0 = rt[2 * i + 1];
+    float ot[2][2][4];
+    if (g.nkeys % 64)
+      local_attention<true, 2>(g, t0, ot_tab, 0, q + img, k_base, vh_base, ktab + i * g.nkp,
+                               vtab + i * g.nkp, ot, lane);
+    else
+      local_attention<false, 2>(g, t0, ot_tab, 0, q + img, k_base, vh_base, ktab + i * g.nkp,
+                                vtab + i * g.nkp, ot, lane);
+    local_lepe<KS, HR, WR>(g, t0, h0, ot_tab, ot_tab + 8, ot, stg, smem + g.off_h, sw,
+                           out + img, lane);
   }
   if (tid == 0) settle_after_timeout();
 }

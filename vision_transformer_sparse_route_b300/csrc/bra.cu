@@ -358,8 +358,64 @@ int check_route(const void *q, const void *k, int B, int H, int W, int C, int S,
   return BRA_OK;
 }
 
+// The per-chunk routing kernel (forward_image.cuh): bf16, C / 64 in {1, 2,
+// 4} CTAs a cluster, at most 64 regions of at most 8 tokens (the maps the
+// local image kernel takes).
+bool plan_route_chunked(int H, int W, int C, int S, int topk, bra::FusedGeom *fg,
+                        size_t *smem) {
+  if (C % 64 || S <= 0 || H % S || W % S) return false;
+  bra::FusedGeom f = {};
+  bra::ImageGeom &a = f.img;
+  a.H = H; a.W = W; a.C = C; a.S = S; a.topk = topk;
+  a.hr = H / S; a.wr = W / S; a.n = a.hr * a.wr; a.R = S * S;
+  a.nc = C / 64;
+  if (a.n > 8 || a.R > 64 || (a.nc != 1 && a.nc != 2 && a.nc != 4)) return false;
+  const int G = route_groups(C, BRA_BF16);
+  if (!G) return false;
+  f.L = 32 / G;
+  f.inv_n = 1.0f / static_cast<float>(a.n);
+  f.rp = (a.R + 3) / 4 * 4;
+  const size_t rows = (size_t)(a.R + a.nc - 1) / a.nc;
+  f.off_qm = 0;
+  f.off_km = f.off_qm + 64 * f.rp * 4;
+  f.off_a = f.off_km + 64 * f.rp * 4;
+  f.off_p = (uint32_t)round_up((size_t)f.off_a + rows * a.R * 4, 16);
+  *smem = (size_t)f.off_p + (size_t)a.R * a.R * 4;
+  *fg = f;
+  return true;
+}
+
+int launch_route_chunked(const void *q, const void *k, int B, const bra::FusedGeom &f,
+                         size_t smem, int32_t *idx, float *aff, cudaStream_t s) {
+  auto kern = f.L == 1   ? bra::bra_route_chunked_kernel<1>
+              : f.L == 2 ? bra::bra_route_chunked_kernel<2>
+                         : bra::bra_route_chunked_kernel<4>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((size_t)B * f.img.nc), 1, 1);
+  cfg.blockDim = dim3(bra::kRouteThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = f.img.nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, static_cast<const __nv_bfloat16 *>(q),
+                                        static_cast<const __nv_bfloat16 *>(k), f, idx, aff));
+}
+
 int launch_route(const void *q, const void *k, int B, int H, int W, int C, int S,
                  int topk, int dtype, int32_t *idx, float *aff, cudaStream_t s) {
+  if (dtype == BRA_BF16) {
+    bra::FusedGeom f;
+    size_t smem;
+    if (plan_route_chunked(H, W, C, S, topk, &f, &smem))
+      return launch_route_chunked(q, k, B, f, smem, idx, aff, s);
+  }
   const int CL = route_cluster(B, S * S, H, W, C, S, topk, dtype);
   bra::RouteGeom g;
   size_t smem;
@@ -591,6 +647,45 @@ bool plan_attend_image(int H, int W, int C, int heads, int S, int topk, int ks,
   return *smem <= kMaxSmemPerBlock;
 }
 
+// The local form of the image kernel: regions of at most 8 tokens; the
+// chunk of the whole image's K (swizzled tile), a zero-bordered V halo with
+// 144-byte rows, the LePE weights, the two key tables and a staging area of
+// n rows per warp in shared memory (Q is read from global memory, and there
+// is no f32 O tile), so that two CTAs share an SM on the stage-3 shape.
+// off_v holds the halo-position key table, off_o the staging area.
+bool plan_attend_image_local(int H, int W, int C, int heads, int S, int topk, int ks,
+                             ImageGeom *g, size_t *smem) {
+  if (C % 64 || C / heads != 32) return false;
+  ImageGeom a = {};
+  a.H = H; a.W = W; a.C = C; a.S = S; a.heads = heads; a.topk = topk;
+  a.hr = H / S; a.wr = W / S; a.n = a.hr * a.wr; a.R = S * S;
+  if (a.n > 8) return false;
+  a.halo_w = W + ks - 1;
+  a.halo_h = H + ks - 1;
+  if (a.halo_w > 256 || a.halo_h > 256) return false;  // TMA box limit
+  a.nc = C / 64;
+  a.nkeys = topk * a.n;
+  a.q_blocks = 1;
+  const size_t tokens = (size_t)H * W;
+  const size_t halo = (size_t)a.halo_w * a.halo_h + 1;  // + the zero row
+  if (halo > 65535) return false;                       // uint16 key tables
+  a.tile = (uint32_t)round_up((tokens + 1) * 128, 1024);
+  a.off_k = 0;
+  a.off_h = a.tile;
+  a.off_w = (uint32_t)round_up((size_t)a.off_h + halo * bra::kHaloPitch, 16);
+  a.nkp = (int)round_up((size_t)a.nkeys, 64);
+  a.off_tab = (uint32_t)round_up((size_t)a.off_w + (size_t)(ks * ks + 1) * 64 * 4, 16);
+  a.off_v = (uint32_t)round_up((size_t)a.off_tab + (size_t)a.R * a.nkp * 2, 16);
+  a.off_o = (uint32_t)round_up((size_t)a.off_v + (size_t)a.R * a.nkp * 2, 16);
+  a.off_rt = (uint32_t)round_up(
+      (size_t)a.off_o + (size_t)bra::kLocalWarps * a.n * bra::kStgStride * 4, 16);
+  a.off_bar = (uint32_t)round_up((size_t)a.off_rt + (size_t)(2 * a.R + 16) * 2, 8);
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt(32.0));
+  *smem = (size_t)a.off_bar + 8 + 1024;  // slack to align the base to 1024 bytes
+  *g = a;
+  return *smem <= kMaxSmemPerBlock;
+}
+
 // The one-launch forward (routing inside the image-resident attend kernel):
 // bf16 maps the image kernel takes, at most 64 regions, and channel counts the
 // routing kernel supports (C / 64 CTAs in a cluster per image: 1, 2 or 4).
@@ -751,6 +846,49 @@ int launch_attend_image_kr(const void *q, const void *k, const void *v,
   cfg.numAttrs = pdl ? 1 : 0;
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, th,
                                         static_cast<__nv_bfloat16 *>(out), idx, w, bias, g));
+}
+
+template <int KS, int HR, int WR>
+int launch_attend_image_local_t(const void *q, const void *k, const void *v,
+                                const int32_t *idx, int B, const float *w,
+                                const float *bias, void *out, const ImageGeom &g,
+                                size_t smem, bool pdl, cudaStream_t s) {
+  CUtensorMap tk, tvh;
+  // the halo's rows are 72 channels: the chunk's 64 and 8 that pad the row
+  // to 144 bytes (past the last channel they read the zero fill)
+  if (!make_map(&tk, k, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map_t(&tvh, v, BRA_BF16, B, g.H, g.W, g.C, g.halo_w, g.halo_h, false,
+                  bra::kHaloPitch / 2))
+    return BRA_ERR_CUDA;
+  auto kern = bra::bra_attend_image_local_kernel<KS, HR, WR>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((size_t)B * g.nc), 1, 1);
+  cfg.blockDim = dim3(bra::kLocalThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tk, tvh,
+                                        static_cast<const __nv_bfloat16 *>(q),
+                                        static_cast<__nv_bfloat16 *>(out), idx, w, bias, g));
+}
+
+// 2 x 2 regions (the stage-3 shape) take the sliding-window LePE, other
+// shapes of at most 8 tokens the token-by-token one
+template <int KS>
+int launch_attend_image_local(const void *q, const void *k, const void *v,
+                              const int32_t *idx, int B, const float *w,
+                              const float *bias, void *out, const ImageGeom &g,
+                              size_t smem, bool pdl, cudaStream_t s) {
+  if (g.hr == 2 && g.wr == 2)
+    return launch_attend_image_local_t<KS, 2, 2>(q, k, v, idx, B, w, bias, out, g, smem, pdl,
+                                                 s);
+  return launch_attend_image_local_t<KS, 0, 0>(q, k, v, idx, B, w, bias, out, g, smem, pdl, s);
 }
 
 template <int KS>
@@ -918,7 +1056,8 @@ int check_attend(const void *q, const void *k, const void *v, const int32_t *idx
   if (dtype == BRA_BF16) {
     ImageGeom gi;
     AttendGeom g;
-    if (!plan_attend_image(H, W, C, heads, S, topk, ks, &gi, &smem) &&
+    if (!plan_attend_image_local(H, W, C, heads, S, topk, ks, &gi, &smem) &&
+        !plan_attend_image(H, W, C, heads, S, topk, ks, &gi, &smem) &&
         !plan_attend_bf16(B, H, W, C, heads, S, topk, ks, &g, &smem))
       return BRA_ERR_UNSUPPORTED;
   } else {
@@ -935,6 +1074,14 @@ int launch_attend(const void *q, const void *k, const void *v, const int32_t *id
   size_t smem;
   if (dtype == BRA_BF16) {
     ImageGeom gi;
+    if (plan_attend_image_local(H, W, C, heads, S, topk, ks, &gi, &smem)) {
+      switch (ks) {
+        case 1: return launch_attend_image_local<1>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+        case 3: return launch_attend_image_local<3>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+        case 5: return launch_attend_image_local<5>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+        default: return launch_attend_image_local<7>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);
+      }
+    }
     if (plan_attend_image(H, W, C, heads, S, topk, ks, &gi, &smem)) {
       switch (ks) {
         case 1: return launch_attend_image_ks<1>(q, k, v, idx, B, w, bias, out, gi, smem, pdl, s);

@@ -90,29 +90,20 @@ __device__ __forceinline__ void region_mean_chunk(const uint8_t *tile, int base,
   }
 }
 
-// Routing of image b by the CTA with chunk cc of a cluster of nc (see
-// above), all its threads. Leaves the whole routing [R][topk] in ridx of
-// every CTA of the cluster; writes this CTA's rows to idx_out.
-__device__ __forceinline__ void route_in_cluster(
-    const ImageGeom &g, const FusedGeom &fg, const uint8_t *smem, float *qm, float *km,
-    float *aff, float *part, int32_t *ridx, const uint16_t *rbase, const uint16_t *toff,
-    int32_t *idx_out, uint64_t *bar_qk, int b, int cc, int nc, int tid, int warp, int lane,
-    cg::cluster_group &cluster) {
+// The rest of the routing by the CTA with chunk cc of a cluster of nc, all
+// its threads, once this chunk's region means are in qm and km (channel-major
+// [64][RP], columns 0 .. R-1): the chunk's partial affinity, a cluster
+// barrier, the full affinity of the rows i with i % nc == cc (partials added
+// in chunk order, from the peers' shared memory), their top-k to idx_out (and
+// the full rows to aff_out when given) and, when ridx is given, into every
+// CTA's copy of the routing; a last cluster barrier.
+__device__ __forceinline__ void route_cluster_rows(const ImageGeom &g, const FusedGeom &fg,
+                                                   float *qm, float *km, float *aff,
+                                                   float *part, int32_t *ridx,
+                                                   int32_t *idx_out, float *aff_out, int b,
+                                                   int cc, int nc, int tid, int warp, int lane,
+                                                   cg::cluster_group &cluster) {
   const int R = g.R, RP = fg.rp;
-  mbar_wait(bar_qk, 0);
-
-  // ---- region means of this chunk's 64 channels: one thread per (tensor,
-  // region, 16-byte chunk); stored channel-major, [64][RP]
-  for (int e = tid; e < 2 * R * 8; e += kRouteThreads) {
-    const int tensor = e / (R * 8), rest = e - tensor * (R * 8);
-    const int r = rest >> 3, chunk = rest & 7;
-    float m[8];
-    region_mean_chunk(tensor ? smem + g.off_k : smem, rbase[r], toff, g.n, chunk, fg.L,
-                      fg.inv_n, m);
-    float *dst = (tensor ? km : qm) + chunk * 8 * RP + r;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) dst[c * RP] = m[c];
-  }
   // the padding columns R .. RP-1 are zero (their products are dropped)
   for (int e = tid; e < 2 * 64 * (RP - R); e += kRouteThreads) {
     const int tensor = e / (64 * (RP - R)), rest = e - tensor * (64 * (RP - R));
@@ -161,6 +152,7 @@ __device__ __forceinline__ void route_in_cluster(
       a = rk == 0 ? p : a + p;
     }
     aff[s * R + j] = a;
+    if (aff_out) aff_out[((size_t)b * R + i) * R + j] = a;
   }
   __syncthreads();
 
@@ -180,18 +172,47 @@ __device__ __forceinline__ void route_in_cluster(
       }
       val[t] = a;
     }
-    select_topk<MAXJ>(val, aff + s * R, R, g.topk, lane, ridx + i * g.topk,
-                      idx_out + ((size_t)b * R + i) * g.topk);
+    select_topk<MAXJ>(val, aff + s * R, R, g.topk, lane,
+                      idx_out + ((size_t)b * R + i) * g.topk, ridx ? ridx + i * g.topk : nullptr);
     __syncwarp();
+    if (!ridx) continue;
     for (int e = lane; e < (nc - 1) * g.topk; e += 32) {
       const int rk = (cc + 1 + e / g.topk) % nc, m = e % g.topk;
       cluster.map_shared_rank(ridx, rk)[i * g.topk + m] = ridx[i * g.topk + m];
     }
   }
-  // every CTA's rows have reached every CTA; no CTA reads a peer's shared
-  // memory after this
+  // every CTA's rows are complete (and have reached every CTA); no CTA reads
+  // a peer's shared memory after this
   cluster_arrive_release();
   cluster_wait_acquire();
+}
+
+
+// Routing of image b by the CTA with chunk cc of a cluster of nc (see
+// above), all its threads. Leaves the whole routing [R][topk] in ridx of
+// every CTA of the cluster; writes this CTA's rows to idx_out.
+__device__ __forceinline__ void route_in_cluster(
+    const ImageGeom &g, const FusedGeom &fg, const uint8_t *smem, float *qm, float *km,
+    float *aff, float *part, int32_t *ridx, const uint16_t *rbase, const uint16_t *toff,
+    int32_t *idx_out, uint64_t *bar_qk, int b, int cc, int nc, int tid, int warp, int lane,
+    cg::cluster_group &cluster) {
+  const int R = g.R, RP = fg.rp;
+  mbar_wait(bar_qk, 0);
+
+  // ---- region means of this chunk's 64 channels: one thread per (tensor,
+  // region, 16-byte chunk); stored channel-major, [64][RP]
+  for (int e = tid; e < 2 * R * 8; e += kRouteThreads) {
+    const int tensor = e / (R * 8), rest = e - tensor * (R * 8);
+    const int r = rest >> 3, chunk = rest & 7;
+    float m[8];
+    region_mean_chunk(tensor ? smem + g.off_k : smem, rbase[r], toff, g.n, chunk, fg.L,
+                      fg.inv_n, m);
+    float *dst = (tensor ? km : qm) + chunk * 8 * RP + r;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) dst[c * RP] = m[c];
+  }
+  route_cluster_rows(g, fg, qm, km, aff, part, ridx, idx_out, nullptr, b, cc, nc, tid, warp,
+                     lane, cluster);
 }
 
 template <int KS, int RB>
@@ -358,6 +379,74 @@ __global__ void __launch_bounds__(kImgThreads, 1)
     image_lepe_item<KS, RB>(g, hb, so, gout, 2 * cp, x, ry0, sw);
   }
   if (tid == 0) settle_after_timeout();
+}
+
+// ---- routing alone (steps a1-a4) for the maps of the local image kernel:
+// bf16, at most 64 regions of at most 8 tokens, C / 64 in {1, 2, 4}. One
+// cluster of C / 64 CTAs per image; CTA cc pools its 64 channels of Q and K
+// straight from global memory (one thread per (tensor, region, 16-byte
+// chunk), the region's tokens loaded together, then summed in the routing
+// kernel's order, as region_mean_chunk does), then route_cluster_rows. The
+// per-chunk form needs no copy of every K mean in every CTA, and its index
+// is the routing kernel's bit for bit.
+template <int L>
+__global__ void __launch_bounds__(kRouteThreads, 2)
+    bra_route_chunked_kernel(const __nv_bfloat16 *__restrict__ q,
+                             const __nv_bfloat16 *__restrict__ k, FusedGeom fg,
+                             int32_t *__restrict__ idx, float *__restrict__ aff_out) {
+  // A dependent grid launched with programmatic serialization may start now;
+  // it waits for this grid before it reads the routing index.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ __align__(16) uint8_t rc_smem[];
+  const ImageGeom &g = fg.img;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int nc = g.nc, cc = (int)cluster.block_rank(), b = blockIdx.x / nc;
+  float *qm = reinterpret_cast<float *>(rc_smem + fg.off_qm);
+  float *km = reinterpret_cast<float *>(rc_smem + fg.off_km);
+  float *aff = reinterpret_cast<float *>(rc_smem + fg.off_a);
+  float *part = reinterpret_cast<float *>(rc_smem + fg.off_p);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = g.R, RP = fg.rp;
+  const size_t img = (size_t)b * g.H * g.W;
+  for (int e = tid; e < 2 * R * 8; e += kRouteThreads) {
+    const int tensor = e / (R * 8), rest = e - tensor * (R * 8);
+    const int r = rest >> 3, chunk = rest & 7;
+    const int y0 = (r / g.S) * g.hr, x0 = (r % g.S) * g.wr;
+    const uint4 *src = reinterpret_cast<const uint4 *>((tensor ? k : q) + cc * 64 + chunk * 8);
+    uint4 v[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < g.n)
+        v[t] = __ldg(src + (img + (size_t)(y0 + t / g.wr) * g.W + x0 + t % g.wr) * (g.C / 8));
+    // partial j (j < L) sums the tokens t = j, j + L, ... in increasing order
+    float2 p[L][4];
+#pragma unroll
+    for (int j = 0; j < L; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) p[j][c] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < g.n) {
+        const uint32_t ws[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          p[t % L][c] = __fadd2_rn(p[t % L][c],
+                                   make_float2(__uint_as_float(__byte_perm(ws[c], 0u, 0x1044u)),
+                                               __uint_as_float(__byte_perm(ws[c], 0u, 0x3244u))));
+      }
+    float *dst = (tensor ? km : qm) + chunk * 8 * RP + r;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      // the partials added pairwise, ((0 + 1) + (2 + 3)), missing ones zero
+      float2 m = p[0][c];
+      if (L == 2) m = __fadd2_rn(p[0][c], p[1][c]);
+      if (L == 4) m = __fadd2_rn(__fadd2_rn(p[0][c], p[1 % L][c]), __fadd2_rn(p[2 % L][c], p[3 % L][c]));
+      dst[(2 * c) * RP] = m.x * fg.inv_n;
+      dst[(2 * c + 1) * RP] = m.y * fg.inv_n;
+    }
+  }
+  route_cluster_rows(g, fg, qm, km, aff, part, nullptr, idx, aff_out, b, cc, nc, tid, warp,
+                     lane, cluster);
 }
 
 }  // namespace bra
