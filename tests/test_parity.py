@@ -160,22 +160,21 @@ def test_host_pipeline_matches_forward(cuda_device):
         assert torch.equal(o, ref.cpu())
 
 
-def test_one_launch_forward_equals_two_kernel_forward(cuda_device):
-    """Small batches of the stage-3 shape run as one kernel (routing inside),
-    large ones as the routing kernel plus the attend kernel; the same images
-    give bit-identical routing and output either way."""
-    wl = bra_synth.WORKLOADS["stage3_bf16"]
-    big = wl.replace(B=64)
-    assert bra.forward_launches(2, wl.H, wl.W, wl.C, wl.heads, wl.S, wl.topk, wl.ks) == 1
-    assert bra.forward_launches(64, wl.H, wl.W, wl.C, wl.heads, wl.S, wl.topk, wl.ks) == 2
-    x = bra_synth.make_inputs(big, seed=17)
-    q, k, v, w, b = device_inputs(big, x, cuda_device)
-    out_big, idx_big = bra.forward(q, k, v, wl.heads, wl.S, wl.topk, w, b)
-    out_two, idx_two = bra.forward(q[:2].contiguous(), k[:2].contiguous(), v[:2].contiguous(),
-                                   wl.heads, wl.S, wl.topk, w, b)
+@pytest.mark.parametrize("B", [64, 2])
+def test_one_launch_forward_equals_two_kernel_forward(B, cuda_device):
+    """The stage-3 shape runs as one kernel (routing inside, clusters of C/64
+    CTAs); the routing kernel followed by the attend kernel gives the same
+    routing and output bit for bit."""
+    wl = bra_synth.WORKLOADS["stage3_bf16"].replace(B=B)
+    assert bra.forward_launches(B, wl.H, wl.W, wl.C, wl.heads, wl.S, wl.topk, wl.ks) == 1
+    x = bra_synth.make_inputs(wl, seed=17)
+    q, k, v, w, b = device_inputs(wl, x, cuda_device)
+    out_one, idx_one = bra.forward(q, k, v, wl.heads, wl.S, wl.topk, w, b)
+    idx_two = bra.route(q, k, wl.S, wl.topk)
+    out_two = bra.attend(q, k, v, idx_two, wl.heads, wl.S, w, b)
     assert bra.device_status() == bra.BRA_OK
-    assert torch.equal(idx_two, idx_big[:2])
-    assert torch.equal(out_two, out_big[:2])
+    assert torch.equal(idx_one, idx_two)
+    assert torch.equal(out_one, out_two)
 
 
 TC_SHAPES = [

@@ -347,24 +347,14 @@ __device__ __forceinline__ void image_lepe_item(const ImageGeom &g, const uint8_
   }
 }
 
-// The common start of the image kernels after thread 0 has issued the tile
-// copies, all threads: stage the chunk's LePE weights (tap-major, bias after
-// them) and build the key table from the routing (the previous grid's
-// output): keys m*n .. m*n+n-1 of query region i are the tokens of routed
-// region idx[b, i, m] in row-major order, as image token numbers in ktab and,
-// when vtab is given, as positions in the V halo tile (image plus a border of
-// ks/2, halo_w wide) in vtab. An out-of-range region's keys and the keys past
-// nkeys (masked) name the zero row after the image's tokens (the zero row
-// after the halo in vtab).
-template <int KS, int NT = kImgThreads>
-__device__ __forceinline__ void image_tables(const ImageGeom &g, float *sw, uint16_t *ktab,
-                                             uint16_t *vtab, const int32_t *__restrict__ idx,
-                                             const float *__restrict__ lepe_w,
-                                             const float *__restrict__ lepe_b, int b, int cc,
-                                             int tid) {
-  constexpr int PAD = KS / 2;
-  // this chunk's LePE weights, read in their [c][tap] order (every load
-  // issued before the first store), stored tap-major
+// The chunk's LePE weights, all threads: read in their [c][tap] order (every
+// load issued before the first store), stored tap-major with the bias after
+// them. sync_before_store runs between the loads and the stores (it lets the
+// weight loads overlap a wait for the previous grid).
+template <int KS, int NT, typename F>
+__device__ __forceinline__ void image_weights(float *sw, const float *__restrict__ lepe_w,
+                                              const float *__restrict__ lepe_b, int cc, int tid,
+                                              F sync_before_store) {
   constexpr int NW = (64 * KS * KS + NT - 1) / NT;
   float wv[NW];
 #pragma unroll
@@ -373,14 +363,7 @@ __device__ __forceinline__ void image_tables(const ImageGeom &g, float *sw, uint
     wv[u] = e < 64 * KS * KS ? __ldg(lepe_w + (size_t)cc * 64 * KS * KS + e) : 0.f;
   }
   const float bv = (tid < 64 && lepe_b) ? __ldg(lepe_b + cc * 64 + tid) : 0.f;
-  grid_dependency_wait();  // the routing comes from the previous grid
-  // the thread's first routing entries (up to four), loaded together before
-  // the weights are stored so that all these loads overlap
-  const int slots = g.R * g.topk;
-  int jpre[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-    jpre[u] = tid + u * NT < slots ? __ldg(idx + (size_t)b * slots + tid + u * NT) : 0;
+  sync_before_store();
 #pragma unroll
   for (int u = 0; u < NW; ++u) {
     const int e = tid + u * NT;
@@ -390,6 +373,33 @@ __device__ __forceinline__ void image_tables(const ImageGeom &g, float *sw, uint
     }
   }
   if (tid < 64) sw[KS * KS * 64 + tid] = bv;
+}
+
+// The key tables of an image from its routing rt ([R][topk]; global memory
+// written by an earlier grid, read through the read-only path, or, with
+// FROM_SMEM, this CTA's shared copy), all threads: keys m*n .. m*n+n-1 of
+// query region i are the tokens of routed region rt[i][m] in row-major
+// order, as image token numbers in ktab and, when vtab is given, as positions
+// in the V halo tile (image plus a border of ks/2, halo_w wide) in vtab. An
+// out-of-range region's keys and the keys past nkeys (masked) name the zero
+// row after the image's tokens (the zero row after the halo in vtab).
+// The thread's first routing entries (up to four), loaded together.
+template <int NT, bool FROM_SMEM>
+__device__ __forceinline__ void prefetch_routing(const ImageGeom &g, const int32_t *rt, int tid,
+                                                 int (&jpre)[4]) {
+  const int slots = g.R * g.topk;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    jpre[u] = tid + u * NT < slots ? (FROM_SMEM ? rt[tid + u * NT] : __ldg(rt + tid + u * NT))
+                                   : 0;
+}
+
+template <int KS, int NT, bool FROM_SMEM>
+__device__ __forceinline__ void image_key_tables(const ImageGeom &g, uint16_t *ktab,
+                                                 uint16_t *vtab, const int32_t *rt,
+                                                 const int (&jpre)[4], int tid) {
+  constexpr int PAD = KS / 2;
+  const int slots = g.R * g.topk;
   const uint16_t zero_row = static_cast<uint16_t>(g.H * g.W);
   const uint16_t zero_pos = static_cast<uint16_t>(g.halo_w * g.halo_h);
   for (int e = tid, u = 0; e < slots; e += NT, ++u) {
@@ -397,7 +407,7 @@ __device__ __forceinline__ void image_tables(const ImageGeom &g, float *sw, uint
     int j = jpre[0];
 #pragma unroll
     for (int v = 1; v < 4; ++v) j = u == v ? jpre[v] : j;
-    if (u >= 4) j = __ldg(idx + (size_t)b * slots + e);
+    if (u >= 4) j = FROM_SMEM ? rt[e] : __ldg(rt + e);
     uint16_t *row = ktab + i * g.nkp + m * g.n;
     uint16_t *vrow = vtab ? vtab + i * g.nkp + m * g.n : nullptr;
     if (j < 0 || j >= g.R) {  // out of range: flag it
@@ -423,6 +433,23 @@ __device__ __forceinline__ void image_tables(const ImageGeom &g, float *sw, uint
     ktab[i * g.nkp + key] = zero_row;
     if (vtab) vtab[i * g.nkp + key] = zero_pos;
   }
+}
+
+// Weights and key tables of the attend kernels (routing from the previous
+// grid; the weight loads overlap the wait for it).
+template <int KS, int NT = kImgThreads>
+__device__ __forceinline__ void image_tables(const ImageGeom &g, float *sw, uint16_t *ktab,
+                                             uint16_t *vtab, const int32_t *__restrict__ idx,
+                                             const float *__restrict__ lepe_w,
+                                             const float *__restrict__ lepe_b, int b, int cc,
+                                             int tid) {
+  const int32_t *rt = idx + (size_t)b * g.R * g.topk;
+  int jpre[4];
+  image_weights<KS, NT>(sw, lepe_w, lepe_b, cc, tid, [&] {
+    grid_dependency_wait();
+    prefetch_routing<NT, false>(g, rt, tid, jpre);
+  });
+  image_key_tables<KS, NT, false>(g, ktab, vtab, rt, jpre, tid);
 }
 
 template <int KS, int RB>

@@ -686,6 +686,39 @@ bool plan_attend_image_local(int H, int W, int C, int heads, int S, int topk, in
   return *smem <= kMaxSmemPerBlock;
 }
 
+// The one-launch forward on the local image kernel's layout: the local
+// kernel's shapes with at most 64 regions and C / 64 in {1, 2, 4}; the
+// routing's scratch (means, this CTA's affinity rows, the chunk's partial
+// affinity) must fit in the V halo's space, and the routing ([R][topk]) and
+// a second mbarrier go after the region tables.
+bool plan_forward_local(int H, int W, int C, int heads, int S, int topk, int ks,
+                        FusedGeom *fg, size_t *smem) {
+  ImageGeom a;
+  size_t s0;
+  if (!plan_attend_image_local(H, W, C, heads, S, topk, ks, &a, &s0)) return false;
+  const int G = route_groups(C, BRA_BF16);
+  if (!G || a.R > 64 || (a.nc != 1 && a.nc != 2 && a.nc != 4)) return false;
+  FusedGeom f = {};
+  f.L = 32 / G;
+  f.inv_n = 1.0f / static_cast<float>(a.n);
+  f.rp = (a.R + 3) / 4 * 4;
+  const size_t rows = (size_t)(a.R + a.nc - 1) / a.nc;
+  f.off_qm = a.off_h;
+  f.off_km = f.off_qm + 64 * f.rp * 4;
+  f.off_a = f.off_km + 64 * f.rp * 4;
+  f.off_p = (uint32_t)round_up((size_t)f.off_a + rows * a.R * 4, 16);
+  const size_t scratch_end = (size_t)f.off_p + (size_t)a.R * a.R * 4;
+  if (scratch_end > (size_t)a.off_h + (size_t)a.halo_w * a.halo_h * bra::kHaloPitch)
+    return false;
+  f.off_ridx = (uint32_t)round_up((size_t)a.off_rt + (size_t)(2 * a.R + 16) * 2, 16);
+  a.off_bar = (uint32_t)round_up((size_t)f.off_ridx + (size_t)a.R * topk * 4, 8);
+  f.off_bar = a.off_bar;
+  f.img = a;
+  *smem = (size_t)a.off_bar + 16 + 1024;  // slack to align the base to 1024 bytes
+  *fg = f;
+  return *smem <= kMaxSmemPerBlock;
+}
+
 // The one-launch forward (routing inside the image-resident attend kernel):
 // bf16 maps the image kernel takes, at most 64 regions, and channel counts the
 // routing kernel supports (C / 64 CTAs in a cluster per image: 1, 2 or 4).
@@ -932,6 +965,57 @@ int launch_forward_image_kr(const void *q, const void *k, const void *v, int32_t
                                         static_cast<__nv_bfloat16 *>(out), idx, w, bias, f));
 }
 
+template <int KS, int HR, int WR, int L>
+int launch_forward_local_t(const void *q, const void *k, const void *v, int32_t *idx, int B,
+                           const float *w, const float *bias, void *out, const FusedGeom &f,
+                           size_t smem, cudaStream_t s) {
+  const ImageGeom &g = f.img;
+  CUtensorMap tk, tvh;
+  if (!make_map(&tk, k, B, g.H, g.W, g.C, g.W, g.H, true) ||
+      !make_map_t(&tvh, v, BRA_BF16, B, g.H, g.W, g.C, g.halo_w, g.halo_h, false,
+                  bra::kHaloPitch / 2))
+    return BRA_ERR_CUDA;
+  auto kern = bra::bra_forward_local_kernel<KS, HR, WR, L>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((size_t)B * g.nc), 1, 1);
+  cfg.blockDim = dim3(bra::kLocalThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = g.nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, tk, tvh,
+                                        static_cast<const __nv_bfloat16 *>(q),
+                                        static_cast<const __nv_bfloat16 *>(k),
+                                        static_cast<__nv_bfloat16 *>(out), idx, w, bias, f));
+}
+
+template <int KS, int HR, int WR>
+int launch_forward_local_l(const void *q, const void *k, const void *v, int32_t *idx, int B,
+                           const float *w, const float *bias, void *out, const FusedGeom &f,
+                           size_t smem, cudaStream_t s) {
+  if (f.L == 1)
+    return launch_forward_local_t<KS, HR, WR, 1>(q, k, v, idx, B, w, bias, out, f, smem, s);
+  if (f.L == 2)
+    return launch_forward_local_t<KS, HR, WR, 2>(q, k, v, idx, B, w, bias, out, f, smem, s);
+  return launch_forward_local_t<KS, HR, WR, 4>(q, k, v, idx, B, w, bias, out, f, smem, s);
+}
+
+template <int KS>
+int launch_forward_local(const void *q, const void *k, const void *v, int32_t *idx, int B,
+                         const float *w, const float *bias, void *out, const FusedGeom &f,
+                         size_t smem, cudaStream_t s) {
+  if (f.img.hr == 2 && f.img.wr == 2)
+    return launch_forward_local_l<KS, 2, 2>(q, k, v, idx, B, w, bias, out, f, smem, s);
+  return launch_forward_local_l<KS, 0, 0>(q, k, v, idx, B, w, bias, out, f, smem, s);
+}
+
 template <int KS>
 int launch_forward_image_ks(const void *q, const void *k, const void *v, int32_t *idx, int B,
                             const float *w, const float *bias, void *out, const FusedGeom &f,
@@ -993,6 +1077,14 @@ int launch_forward(const void *q, const void *k, const void *v, int B, int H, in
                    int dtype, int32_t *idx, void *out, cudaStream_t s) {
   FusedGeom f;
   size_t smem;
+  if (dtype == BRA_BF16 && plan_forward_local(H, W, C, heads, S, topk, ks, &f, &smem)) {
+    switch (ks) {
+      case 1: return launch_forward_local<1>(q, k, v, idx, B, w, bias, out, f, smem, s);
+      case 3: return launch_forward_local<3>(q, k, v, idx, B, w, bias, out, f, smem, s);
+      case 5: return launch_forward_local<5>(q, k, v, idx, B, w, bias, out, f, smem, s);
+      default: return launch_forward_local<7>(q, k, v, idx, B, w, bias, out, f, smem, s);
+    }
+  }
   if (dtype == BRA_BF16 && plan_forward_image(H, W, C, heads, S, topk, ks, &f, &smem) &&
       forward_image_one_wave(B, f, smem)) {
     switch (ks) {
@@ -1015,6 +1107,8 @@ int forward_launches(int B, int H, int W, int C, int heads, int S, int topk, int
                      int dtype) {
   FusedGeom f;
   size_t smem;
+  if (dtype == BRA_BF16 && plan_forward_local(H, W, C, heads, S, topk, ks, &f, &smem))
+    return 1;
   return (dtype == BRA_BF16 && plan_forward_image(H, W, C, heads, S, topk, ks, &f, &smem) &&
           forward_image_one_wave(B, f, smem))
              ? 1

@@ -97,6 +97,7 @@ __device__ __forceinline__ void region_mean_chunk(const uint8_t *tile, int base,
 // in chunk order, from the peers' shared memory), their top-k to idx_out (and
 // the full rows to aff_out when given) and, when ridx is given, into every
 // CTA's copy of the routing; a last cluster barrier.
+template <int NT = kRouteThreads>
 __device__ __forceinline__ void route_cluster_rows(const ImageGeom &g, const FusedGeom &fg,
                                                    float *qm, float *km, float *aff,
                                                    float *part, int32_t *ridx,
@@ -105,7 +106,7 @@ __device__ __forceinline__ void route_cluster_rows(const ImageGeom &g, const Fus
                                                    cg::cluster_group &cluster) {
   const int R = g.R, RP = fg.rp;
   // the padding columns R .. RP-1 are zero (their products are dropped)
-  for (int e = tid; e < 2 * 64 * (RP - R); e += kRouteThreads) {
+  for (int e = tid; e < 2 * 64 * (RP - R); e += NT) {
     const int tensor = e / (64 * (RP - R)), rest = e - tensor * (64 * (RP - R));
     (tensor ? km : qm)[(rest / (RP - R)) * RP + R + rest % (RP - R)] = 0.f;
   }
@@ -114,28 +115,33 @@ __device__ __forceinline__ void route_cluster_rows(const ImageGeom &g, const Fus
   // ---- partial affinity over this chunk: one thread per 4 x 4 tile (rows
   // i0.., columns j0..), sixteen FMA chains in channel order
   const int tiles = RP / 4;
-  for (int t = tid; t < tiles * tiles; t += kRouteThreads) {
+  for (int t = tid; t < tiles * tiles; t += NT) {
     const int i0 = (t / tiles) * 4, j0 = (t % tiles) * 4;
-    float acc[4][4];
+    // the chains in pairs (columns j0 + 2h, j0 + 2h + 1): each half of a
+    // paired FMA rounds as a single one
+    float2 acc[4][2];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+    for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
 #pragma unroll 4
     for (int c = 0; c < 64; ++c) {
       const float4 q4 = *reinterpret_cast<const float4 *>(qm + c * RP + i0);
       const float4 k4 = *reinterpret_cast<const float4 *>(km + c * RP + j0);
-      const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+      const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+      const float2 k01 = make_float2(k4.x, k4.y), k23 = make_float2(k4.z, k4.w);
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) acc[r][c2] = fmaf(qv[r], kv[c2], acc[r][c2]);
+      for (int r = 0; r < 4; ++r) {
+        const float2 q2 = make_float2(qv[r], qv[r]);
+        acc[r][0] = __ffma2_rn(q2, k01, acc[r][0]);
+        acc[r][1] = __ffma2_rn(q2, k23, acc[r][1]);
+      }
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < 4; ++r) {
+      const float a[4] = {acc[r][0].x, acc[r][0].y, acc[r][1].x, acc[r][1].y};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        if (i0 + r < R && j0 + c < R) part[(i0 + r) * R + j0 + c] = acc[r][c];
+        if (i0 + r < R && j0 + c < R) part[(i0 + r) * R + j0 + c] = a[c];
+    }
   }
   cluster_arrive_release();
   cluster_wait_acquire();  // every chunk's partial affinity is complete
@@ -143,7 +149,7 @@ __device__ __forceinline__ void route_cluster_rows(const ImageGeom &g, const Fus
   // ---- the full affinity of this CTA's rows i = cc, cc + nc, ...: partials
   // added in chunk order
   const int ro = (R - cc + nc - 1) / nc;
-  for (int e = tid; e < ro * R; e += kRouteThreads) {
+  for (int e = tid; e < ro * R; e += NT) {
     const int s = e / R, j = e - s * R;
     const int i = cc + nc * s;
     float a = 0.f;
@@ -158,7 +164,7 @@ __device__ __forceinline__ void route_cluster_rows(const ImageGeom &g, const Fus
 
   // ---- top-k of this CTA's rows (one warp per row), to global memory and
   // into every CTA's copy of the routing
-  for (int s = warp; s < ro; s += kRouteWarps) {
+  for (int s = warp; s < ro; s += (NT / 32)) {
     const int i = cc + nc * s;
     constexpr int MAXJ = 2;  // at most 64 regions
     float val[MAXJ];
@@ -381,34 +387,18 @@ __global__ void __launch_bounds__(kImgThreads, 1)
   if (tid == 0) settle_after_timeout();
 }
 
-// ---- routing alone (steps a1-a4) for the maps of the local image kernel:
-// bf16, at most 64 regions of at most 8 tokens, C / 64 in {1, 2, 4}. One
-// cluster of C / 64 CTAs per image; CTA cc pools its 64 channels of Q and K
-// straight from global memory (one thread per (tensor, region, 16-byte
+// The region means of chunk cc's 64 channels of Q and K of image b, read
+// from global memory, all NT threads: one thread per (tensor, region, 16-byte
 // chunk), the region's tokens loaded together, then summed in the routing
-// kernel's order, as region_mean_chunk does), then route_cluster_rows. The
-// per-chunk form needs no copy of every K mean in every CTA, and its index
-// is the routing kernel's bit for bit.
-template <int L>
-__global__ void __launch_bounds__(kRouteThreads, 2)
-    bra_route_chunked_kernel(const __nv_bfloat16 *__restrict__ q,
-                             const __nv_bfloat16 *__restrict__ k, FusedGeom fg,
-                             int32_t *__restrict__ idx, float *__restrict__ aff_out) {
-  // A dependent grid launched with programmatic serialization may start now;
-  // it waits for this grid before it reads the routing index.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  extern __shared__ __align__(16) uint8_t rc_smem[];
-  const ImageGeom &g = fg.img;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int nc = g.nc, cc = (int)cluster.block_rank(), b = blockIdx.x / nc;
-  float *qm = reinterpret_cast<float *>(rc_smem + fg.off_qm);
-  float *km = reinterpret_cast<float *>(rc_smem + fg.off_km);
-  float *aff = reinterpret_cast<float *>(rc_smem + fg.off_a);
-  float *part = reinterpret_cast<float *>(rc_smem + fg.off_p);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// kernel's order (as region_mean_chunk does); stored channel-major, [64][RP].
+template <int L, int NT>
+__device__ __forceinline__ void chunk_means(const __nv_bfloat16 *__restrict__ q,
+                                            const __nv_bfloat16 *__restrict__ k,
+                                            const ImageGeom &g, const FusedGeom &fg, float *qm,
+                                            float *km, int b, int cc, int tid) {
   const int R = g.R, RP = fg.rp;
   const size_t img = (size_t)b * g.H * g.W;
-  for (int e = tid; e < 2 * R * 8; e += kRouteThreads) {
+  for (int e = tid; e < 2 * R * 8; e += NT) {
     const int tensor = e / (R * 8), rest = e - tensor * (R * 8);
     const int r = rest >> 3, chunk = rest & 7;
     const int y0 = (r / g.S) * g.hr, x0 = (r % g.S) * g.wr;
@@ -445,8 +435,138 @@ __global__ void __launch_bounds__(kRouteThreads, 2)
       dst[(2 * c + 1) * RP] = m.y * fg.inv_n;
     }
   }
+}
+
+// ---- routing alone (steps a1-a4) for the maps of the local image kernel:
+// bf16, at most 64 regions of at most 8 tokens, C / 64 in {1, 2, 4}. One
+// cluster of C / 64 CTAs per image; CTA cc pools its 64 channels of Q and K
+// straight from global memory (one thread per (tensor, region, 16-byte
+// chunk), the region's tokens loaded together, then summed in the routing
+// kernel's order, as region_mean_chunk does), then route_cluster_rows. The
+// per-chunk form needs no copy of every K mean in every CTA, and its index
+// is the routing kernel's bit for bit.
+template <int L>
+__global__ void __launch_bounds__(kRouteThreads, 2)
+    bra_route_chunked_kernel(const __nv_bfloat16 *__restrict__ q,
+                             const __nv_bfloat16 *__restrict__ k, FusedGeom fg,
+                             int32_t *__restrict__ idx, float *__restrict__ aff_out) {
+  // A dependent grid launched with programmatic serialization may start now;
+  // it waits for this grid before it reads the routing index.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ __align__(16) uint8_t rc_smem[];
+  const ImageGeom &g = fg.img;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int nc = g.nc, cc = (int)cluster.block_rank(), b = blockIdx.x / nc;
+  float *qm = reinterpret_cast<float *>(rc_smem + fg.off_qm);
+  float *km = reinterpret_cast<float *>(rc_smem + fg.off_km);
+  float *aff = reinterpret_cast<float *>(rc_smem + fg.off_a);
+  float *part = reinterpret_cast<float *>(rc_smem + fg.off_p);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  chunk_means<L, kRouteThreads>(q, k, g, fg, qm, km, b, cc, tid);
   route_cluster_rows(g, fg, qm, km, aff, part, nullptr, idx, aff_out, b, cc, nc, tid, warp,
                      lane, cluster);
+}
+
+// ---- the whole forward in one launch on the local image kernel's layout
+// (two CTAs per SM, so that every image's cluster is resident at once on the
+// stage-3 shape): one cluster of C / 64 CTAs of kLocalThreads per image. CTA
+// cc issues the TMA copy of its chunk of K, stages the LePE weights, routes
+// the image with its peers (chunk_means from global memory, then
+// route_cluster_rows, which leaves the whole routing in every CTA), then
+// copies the V halo into the space the routing used, builds the key tables
+// from its copy of the routing and runs the local kernel's attention and
+// LePE (attend_image.cuh).
+template <int KS, int HR, int WR, int L>
+__global__ void __launch_bounds__(kLocalThreads, 2)
+    bra_forward_local_kernel(const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_vh,
+                             const __nv_bfloat16 *__restrict__ q,
+                             const __nv_bfloat16 *__restrict__ k,
+                             __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ idx_out,
+                             const float *__restrict__ lepe_w, const float *__restrict__ lepe_b,
+                             FusedGeom fg) {
+  extern __shared__ uint8_t image_smem_raw[];
+  uint8_t *smem = image_smem_raw + ((1024u - (smem_u32(image_smem_raw) & 1023u)) & 1023u);
+  const ImageGeom &g = fg.img;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int nc = g.nc, cc = (int)cluster.block_rank(), b = blockIdx.x / nc;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float *sw = reinterpret_cast<float *>(smem + g.off_w);
+  uint16_t *ktab = reinterpret_cast<uint16_t *>(smem + g.off_tab);
+  uint16_t *vtab = reinterpret_cast<uint16_t *>(smem + g.off_v);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + g.off_bar);  // [0] K, [1] V halo
+  // the routing's scratch lies in the halo's space (the halo is copied after
+  // the routing); the routing itself ([R][topk]) has its own
+  float *qm = reinterpret_cast<float *>(smem + fg.off_qm);
+  float *km = reinterpret_cast<float *>(smem + fg.off_km);
+  float *aff = reinterpret_cast<float *>(smem + fg.off_a);
+  float *part = reinterpret_cast<float *>(smem + fg.off_p);
+  int32_t *ridx = reinterpret_cast<int32_t *>(smem + fg.off_ridx);
+  constexpr int PAD = KS / 2;
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar[0], g.H * g.W * 128);
+    tma_load_4d(smem + g.off_k, &tm_k, &bar[0], cc * 64, 0, 0, b);
+  }
+  // the zero rows after the K tile and after the halo (no copy writes them;
+  // the routing's scratch ends before the halo's zero row)
+  if (tid < 8)
+    *reinterpret_cast<uint4 *>(smem + g.off_k + g.H * g.W * 128 + tid * 16) =
+        make_uint4(0, 0, 0, 0);
+  else if (tid < 17)
+    *reinterpret_cast<uint4 *>(smem + g.off_h + g.halo_w * g.halo_h * kHaloPitch +
+                               (tid - 8) * 16) = make_uint4(0, 0, 0, 0);
+  image_weights<KS, kLocalThreads>(sw, lepe_w, lepe_b, cc, tid, [] {});
+  uint16_t *rt = reinterpret_cast<uint16_t *>(smem + g.off_rt);
+  uint16_t *ot_tab = rt + 2 * g.R;
+  for (int e = tid; e < g.R + g.n; e += kLocalThreads) {
+    if (e < g.R) {
+      const int y0 = (e / g.S) * g.hr, x0 = (e % g.S) * g.wr;
+      rt[2 * e] = static_cast<uint16_t>(y0 * g.W + x0);
+      rt[2 * e + 1] = static_cast<uint16_t>(y0 * g.halo_w + x0);
+    } else {
+      const int r = e - g.R, dy = r / g.wr, dx = r % g.wr;
+      ot_tab[r] = static_cast<uint16_t>(dy * g.W + dx);
+      ot_tab[8 + r] = static_cast<uint16_t>(dy * g.halo_w + dx);
+    }
+  }
+
+  // ---- routing (steps a1-a4)
+  chunk_means<L, kLocalThreads>(q, k, g, fg, qm, km, b, cc, tid);
+  route_cluster_rows<kLocalThreads>(g, fg, qm, km, aff, part, ridx, idx_out, nullptr, b, cc,
+                                    nc, tid, warp, lane, cluster);
+  __syncthreads();  // no thread here or in a peer touches the scratch any more
+  if (tid == 0) {
+    fence_async_shared();  // the scratch's generic accesses before the copy
+    mbar_arrive_expect_tx(&bar[1], g.halo_w * g.halo_h * kHaloPitch);
+    tma_load_4d(smem + g.off_h, &tm_vh, &bar[1], cc * 64, -PAD, -PAD, b);
+  }
+  int jpre[4];
+  prefetch_routing<kLocalThreads, true>(g, ridx, tid, jpre);
+  image_key_tables<KS, kLocalThreads, true>(g, ktab, vtab, ridx, jpre, tid);
+  __syncthreads();
+  mbar_wait(&bar[0], 0);
+  mbar_wait(&bar[1], 0);
+
+  // ---- attention + LePE (steps a5-a7)
+  const uint32_t k_base = smem_u32(smem + g.off_k), vh_base = smem_u32(smem + g.off_h);
+  float *stg = reinterpret_cast<float *>(smem + g.off_o) + warp * g.n * kStgStride;
+  const size_t img = (size_t)b * g.H * g.W * g.C + cc * 64;
+  for (int i = warp; i < g.R; i += kLocalWarps) {
+    const int t0 = rt[2 * i], h0 = rt[2 * i + 1];
+    float ot[2][2][4];
+    if (g.nkeys % 64)
+      local_attention<true, 2>(g, t0, ot_tab, 0, q + img, k_base, vh_base, ktab + i * g.nkp,
+                               vtab + i * g.nkp, ot, lane);
+    else
+      local_attention<false, 2>(g, t0, ot_tab, 0, q + img, k_base, vh_base, ktab + i * g.nkp,
+                                vtab + i * g.nkp, ot, lane);
+    local_lepe<KS, HR, WR>(g, t0, h0, ot_tab, ot_tab + 8, ot, stg, smem + g.off_h, sw,
+                           out + img, lane);
+  }
+  if (tid == 0) settle_after_timeout();
 }
 
 }  // namespace bra
