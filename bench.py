@@ -103,9 +103,14 @@ def kernel_sources(kernel: str, workload: str) -> list:
     "attend") runs as for a workload: the kernel's own header and the headers
     it includes. A recorded DRAM byte count stays valid while these are
     unchanged."""
-    if kernel == "route":
-        return ["route.cuh", "ptx.cuh"]
     wl = bra_synth.WORKLOADS[workload]
+    small = wl.dtype == "bf16" and wl.H // wl.S * (wl.W // wl.S) <= 8
+    if kernel == "route":
+        if small and wl.S * wl.S <= 64 and wl.C // 64 in (1, 2, 4) and wl.C % 64 == 0:
+            # the per-chunk routing kernel of the small-map path
+            return ["forward_image.cuh", "attend_image.cuh", "attend_bf16.cuh", "route.cuh",
+                    "ptx.cuh"]
+        return ["route.cuh", "ptx.cuh"]
     if wl.dtype == "f32":
         return ["attend_f32.cuh", "ptx.cuh"]
     if wl.H // wl.S * (wl.W // wl.S) < 16:  # regions under 16 tokens: image-resident kernel

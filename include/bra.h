@@ -94,8 +94,10 @@ int bra_route(const void *q, const void *k, int B, int H, int W, int C, int S,
  * d <= 64; shared-memory footprint within the per-block limit. Otherwise
  * BRA_ERR_UNSUPPORTED. bf16 maps whose regions hold fewer than 16 tokens and
  * whose whole image fits in shared memory one 64-channel chunk at a time
- * (about 250 tokens) run an image-resident kernel; the others a persistent
- * kernel over query regions. The choice depends on the shape only.
+ * (about 250 tokens) run an image-resident kernel (regions of at most 8
+ * tokens its local form: K and a zero-bordered V halo in shared memory, two
+ * CTAs to an SM); the others a persistent kernel over query regions. The
+ * choice depends on the shape only.
  */
 int bra_attend(const void *q, const void *k, const void *v, const int32_t *idx,
                int B, int H, int W, int C, int heads, int S, int topk,
@@ -125,11 +127,12 @@ int bra_attend_tc(const void *q, const void *k, const void *v, const int32_t *id
  *   idx_workspace  device buffer of bra_idx_workspace_bytes(B, S, topk)
  *                  bytes; receives the routing index, the same bit for bit
  *                  as bra_route's.
- * Other arguments as above. bf16 maps that the image-resident attend kernel
- * takes, with at most 64 regions, C in {64, 128, 256} and few enough images
- * that one cluster of C / 64 CTAs per image is resident at once on the device,
- * run as one kernel with the routing computed inside it; other problems run
- * the routing kernel and then the attend kernel.
+ * Other arguments as above. bf16 maps with at most 64 regions and C in {64,
+ * 128, 256} that the image-resident attend kernel takes run as one kernel
+ * with the routing computed inside it (one cluster of C / 64 CTAs per
+ * image): always for regions of at most 8 tokens, and for regions of 9 to 15
+ * tokens when every image's cluster is resident at once on the device. Other
+ * problems run the routing kernel and then the attend kernel.
  */
 int bra_forward(const void *q, const void *k, const void *v, int B, int H,
                 int W, int C, int heads, int S, int topk, const float *lepe_w,

@@ -49,7 +49,9 @@ def test_sources_digest_covers_the_kernel_sources(tmp_path, monkeypatch):
 
 
 def test_kernel_sources_follow_the_kernel_each_workload_runs():
-    assert bench.kernel_sources("route", "stage3_bf16") == ["route.cuh", "ptx.cuh"]
+    assert bench.kernel_sources("route", "stage1_bf16") == ["route.cuh", "ptx.cuh"]
+    assert bench.kernel_sources("route", "tiny_f32") == ["route.cuh", "ptx.cuh"]
+    assert bench.kernel_sources("route", "stage3_bf16")[0] == "forward_image.cuh"
     assert bench.kernel_sources("attend", "tiny_f32")[0] == "attend_f32.cuh"
     assert bench.kernel_sources("attend", "stage3_bf16")[0] == "attend_image.cuh"
     for name in ("stage1_bf16", "stage2_bf16", "seg512_bf16"):
