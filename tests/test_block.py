@@ -140,11 +140,14 @@ def test_linear_matches_oracle(M, K, N, with_res, cuda_device):
         assert torch.equal(r2, y)
 
 
-def test_dwconv_gelu_matches_oracle(cuda_device):
-    rng = np.random.default_rng(21)
-    h = bf16(rng.standard_normal((2, 7, 9, 192)), cuda_device)  # ragged map, 3C channels
-    w = (rng.standard_normal((192, 3, 3)) / 3).astype(np.float32)
-    b = (0.1 * rng.standard_normal(192)).astype(np.float32)
+@pytest.mark.parametrize("Ch,H,W", [(192, 7, 9), (384, 17, 8), (264, 9, 20), (192, 56, 56)])
+def test_dwconv_gelu_matches_oracle(Ch, H, W, cuda_device):
+    # 192: one TMA box of the input tile; 384: two boxes; 264: the unstaged
+    # kernel (above 256 channels and not a multiple of 16); ragged maps
+    rng = np.random.default_rng(21 + Ch)
+    h = bf16(rng.standard_normal((2, H, W, Ch)), cuda_device)
+    w = (rng.standard_normal((Ch, 3, 3)) / 3).astype(np.float32)
+    b = (0.1 * rng.standard_normal(Ch)).astype(np.float32)
     y = bra.dwconv_gelu(h, torch.from_numpy(w).to(cuda_device), torch.from_numpy(b).to(cuda_device))
     ref = oracle.gelu(oracle.lepe(f64(h), w, b))
     assert np.all(np.abs(f64(y) - ref) <= ln_bound(ref))

@@ -9,6 +9,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace bra {
 
 constexpr int kLnThreads = 256;
@@ -155,6 +157,117 @@ __global__ void __launch_bounds__(kDwMaxThreads, 1)
         make_uint4(pack2_bf16(o[0], o[1]), pack2_bf16(o[2], o[3]), pack2_bf16(o[4], o[5]),
                    pack2_bf16(o[6], o[7]));
   }
+}
+
+// The same convolution and GELU, persistent, with the input staged in shared
+// memory: a CTA takes the tiles blockIdx.x, + gridDim.x, ... in turn; thread
+// 0 copies each tile's (8 + 2) x (8 + 2) input tokens (NB boxes of Ch / NB
+// channels, one TMA copy each, zero filled outside the image, which is the
+// padding) into one of two buffers, the next tile's copy in flight while the
+// current one is computed. Every thread (chunk j, column cx) keeps its
+// channels' weights in registers for all the tiles and slides down a tile's
+// rows reading its three input columns from shared memory (consecutive
+// threads read consecutive 16-byte chunks of a token). The FMAs of a channel
+// pair are paired (each half rounds as a single FMA), in the unstaged
+// kernel's order.
+constexpr int kDwIn = kDwTile + 2;  // input tile side
+
+template <int NB>
+__global__ void __launch_bounds__(kDwMaxThreads, 1)
+    bra_dwconv_gelu_tma_kernel(const __grid_constant__ CUtensorMap tm_h,
+                               const float *__restrict__ w, const float *__restrict__ bias,
+                               int B, int H, int W, int Ch, __nv_bfloat16 *__restrict__ y) {
+  extern __shared__ uint8_t dw_smem_raw[];
+  uint8_t *smem = dw_smem_raw + ((128u - (smem_u32(dw_smem_raw) & 127u)) & 127u);
+  const int cb = Ch / NB;  // channels a box
+  const uint32_t box_bytes = kDwIn * kDwIn * cb * 2, buf_bytes = NB * box_bytes;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 2 * buf_bytes);  // one a buffer
+  const int nch = Ch / 8;
+  const int j = threadIdx.x % nch, cx = threadIdx.x / nch;  // chunk, tile column
+  const int tiles_x = (W + kDwTile - 1) / kDwTile, tiles_y = (H + kDwTile - 1) / kDwTile;
+  const int tiles = B * tiles_x * tiles_y;
+  auto issue = [&](int tile, int buf) {
+    const int b = tile / (tiles_x * tiles_y);
+    const int x0 = (tile % tiles_x) * kDwTile, y0 = ((tile / tiles_x) % tiles_y) * kDwTile;
+    mbar_arrive_expect_tx(&bar[buf], buf_bytes);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+      tma_load_4d(smem + buf * buf_bytes + nb * box_bytes, &tm_h, &bar[buf], nb * cb, x0 - 1,
+                  y0 - 1, b);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+    if ((int)blockIdx.x < tiles) issue(blockIdx.x, 0);
+  }
+  const int c0 = 8 * j;
+  float2 wt[9][4], bi[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int tap = 0; tap < 9; ++tap)
+      wt[tap][i] = make_float2(__ldg(w + (size_t)(c0 + 2 * i) * 9 + tap),
+                               __ldg(w + (size_t)(c0 + 2 * i + 1) * 9 + tap));
+    bi[i] = bias ? make_float2(__ldg(bias + c0 + 2 * i), __ldg(bias + c0 + 2 * i + 1))
+                 : make_float2(0.f, 0.f);
+  }
+  // chunk j's 16 bytes of input token (row 0, column cx) of a buffer
+  const uint32_t col_ofs = (c0 / cb) * box_bytes + (uint32_t)(cx * cb + c0 % cb) * 2;
+  int it = 0;
+  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
+    const int buf = it & 1;
+    __syncthreads();  // every thread is done with the other buffer (and the barriers exist)
+    if (threadIdx.x == 0 && tile + (int)gridDim.x < tiles) {
+      fence_async_shared();  // its reads before the copy that overwrites it
+      issue(tile + gridDim.x, buf ^ 1);
+    }
+    mbar_wait(&bar[buf], (it >> 1) & 1);
+    const int b = tile / (tiles_x * tiles_y);
+    const int x0 = (tile % tiles_x) * kDwTile, y0 = ((tile / tiles_x) % tiles_y) * kDwTile;
+    const int x = x0 + cx;
+    if (x >= W) continue;
+    float2 acc[kDwTile][4];
+#pragma unroll
+    for (int r = 0; r < kDwTile; ++r)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[r][i] = bi[i];
+    const uint8_t *col = smem + buf * buf_bytes + col_ofs;
+#pragma unroll
+    for (int ir = 0; ir < kDwIn; ++ir) {
+#pragma unroll
+      for (int dx = 0; dx < 3; ++dx) {
+        float v[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4 *>(col + (size_t)(ir * kDwIn + dx) * cb * 2),
+                      v);
+#pragma unroll
+        for (int dy = 0; dy < 3; ++dy) {
+          const int r = ir - dy;
+          if (r < 0 || r >= kDwTile) continue;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            acc[r][i] = __ffma2_rn(wt[dy * 3 + dx][i], make_float2(v[2 * i], v[2 * i + 1]),
+                                   acc[r][i]);
+        }
+      }
+    }
+    __nv_bfloat16 *yb = y + (size_t)b * H * W * Ch + c0;
+#pragma unroll
+    for (int r = 0; r < kDwTile; ++r) {
+      const int oy = y0 + r;
+      if (oy >= H) break;
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        o[2 * i] = 0.5f * acc[r][i].x * (1.0f + erff(acc[r][i].x * 0.70710678118654752f));
+        o[2 * i + 1] = 0.5f * acc[r][i].y * (1.0f + erff(acc[r][i].y * 0.70710678118654752f));
+      }
+      reinterpret_cast<uint4 *>(yb + ((size_t)oy * W + x) * Ch)[0] =
+          make_uint4(pack2_bf16(o[0], o[1]), pack2_bf16(o[2], o[3]), pack2_bf16(o[4], o[5]),
+                     pack2_bf16(o[6], o[7]));
+    }
+  }
+  if (threadIdx.x == 0) settle_after_timeout();
 }
 
 }  // namespace bra

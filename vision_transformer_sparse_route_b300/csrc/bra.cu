@@ -1376,9 +1376,35 @@ int bra_dwconv_gelu(const void *h, const float *w, const float *bias, int B, int
                           ((W + bra::kDwTile - 1) / bra::kDwTile);
   if (tiles > 0x7fffffffll) return BRA_ERR_UNSUPPORTED;
   (void)cudaGetLastError();
-  auto kern = bra::bra_dwconv_gelu_kernel;
-  kern<<<(unsigned)tiles, (unsigned)(Ch / 8 * bra::kDwTile), 0,
-         static_cast<cudaStream_t>(stream)>>>(
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned threads = (unsigned)(Ch / 8 * bra::kDwTile);
+  // the input tile staged by TMA: one box of all channels up to 256, two of
+  // Ch / 2 up to 384 (a box holds at most 256 elements a row)
+  const int nb = Ch <= 256 ? 1 : (Ch % 16 == 0 ? 2 : 0);
+  CUtensorMap tm;
+  if (nb && make_map_t(&tm, h, BRA_BF16, B, H, W, Ch, bra::kDwIn, bra::kDwIn, false, Ch / nb)) {
+    // two input buffers and their mbarriers; a persistent grid of as many
+    // CTAs as are resident at once
+    const size_t smem = (size_t)2 * bra::kDwIn * bra::kDwIn * Ch * 2 + 16 + 128;
+    const void *kern = nb == 1 ? reinterpret_cast<const void *>(bra::bra_dwconv_gelu_tma_kernel<1>)
+                               : reinterpret_cast<const void *>(bra::bra_dwconv_gelu_tma_kernel<2>);
+    if (allow_smem(kern, smem) != cudaSuccess) return BRA_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, (int)threads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      return BRA_ERR_CUDA;
+    const unsigned grid = (unsigned)std::min<long long>(tiles, (long long)per_sm * sm_count());
+    __nv_bfloat16 *yo = static_cast<__nv_bfloat16 *>(y);
+    if (nb == 1)
+      bra::bra_dwconv_gelu_tma_kernel<1><<<grid, threads, smem, st>>>(tm, w, bias, B, H, W, Ch,
+                                                                       yo);
+    else
+      bra::bra_dwconv_gelu_tma_kernel<2><<<grid, threads, smem, st>>>(tm, w, bias, B, H, W, Ch,
+                                                                       yo);
+    return cuda_status(cudaGetLastError());
+  }
+  bra::bra_dwconv_gelu_kernel<<<(unsigned)tiles, threads, 0, st>>>(
       static_cast<const __nv_bfloat16 *>(h), w, bias, B, H, W, Ch,
       static_cast<__nv_bfloat16 *>(y));
   return cuda_status(cudaGetLastError());
