@@ -51,6 +51,8 @@ def _load():
             "oracle_layer_norm": [P, I, I, P, P, ctypes.c_double, P],
             "oracle_linear": [P, I, I, P, I, P, P],
             "oracle_gelu": [P, ctypes.c_size_t, P],
+            "oracle_attend_backward": [P, P, P, P, I, I, I, I, I, I, I, P, I, P, P, P, P, P,
+                                       P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -157,6 +159,20 @@ def attend(q, k, v, idx, heads: int, S: int, w, bias, threads: int = 1) -> np.nd
                                  idx.shape[-1], _p(w), _p(bias), w.shape[-1], _p(out),
                                  threads), "attend")
     return out
+
+
+def attend_backward(q, k, v, idx, heads: int, S: int, w, dout):
+    """Gradients of attend's output (attention + LePE, the routing fixed) for
+    the upstream gradient dout: (dq, dk, dv, dw, db)."""
+    q, k, v, idx, w, dout = _f64(q), _f64(k), _f64(v), _i32(idx), _f64(w), _f64(dout)
+    B, H, W, C = q.shape
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    dw = np.empty_like(w)
+    db = np.empty(C)
+    _check(_load().oracle_attend_backward(_p(q), _p(k), _p(v), _p(idx), B, H, W, C, heads, S,
+                                          idx.shape[-1], _p(w), w.shape[-1], _p(dout), _p(dq),
+                                          _p(dk), _p(dv), _p(dw), _p(db)), "attend_backward")
+    return dq, dk, dv, dw, db
 
 
 def forward(q, k, v, heads: int, S: int, topk: int, w, bias, threads: int = 1):

@@ -51,6 +51,11 @@
  *     convolution with bias and zero padding 1 in the 3C-channel hidden
  *     layer, the exact (erf) GELU of nn.GELU, fc2 = Linear(3C, C).
  *
+ *   - The backward of attend holds the routing fixed: [P2] §4's TopkRouting
+ *     with diff_routing=False passes no gradient to the routing, so the
+ *     index is a constant of the attention and only q, k, v and the LePE's
+ *     weight and bias receive gradients.
+ *
  * All tensors are contiguous channels-last [B, H, W, C] arrays of double.
  * Functions return 0 on success and 1 on an invalid argument.
  */
@@ -472,5 +477,90 @@ int oracle_linear(const double *x, int M, int K, const double *w, int N, const d
 int oracle_gelu(const double *x, size_t n, double *y) {
   if (!x || !y) return ORACLE_EINVAL;
   for (size_t i = 0; i < n; ++i) y[i] = 0.5 * x[i] * (1.0 + erf(x[i] / sqrt(2.0)));
+  return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Backward of attend (out = attention + LePE(v), the routing fixed; see the
+ * readings above). dout is dL/dout. For one query (its row of the softmax P
+ * over the k*n routed keys, its attention output O, D = dout . O):
+ *   dv[key] += P[key] dout                         (O = sum P v)
+ *   dS[key]  = P[key] (dout . v[key] - D)          (softmax)
+ *   dq      += scale dS[key] k[key],   dk[key] += scale dS[key] q
+ * and for the LePE (cross-correlation, zero padding):
+ *   dv[y][x][c] += sum_{u,s} w[c][u][s] dout[y - u + pad][x - s + pad][c]
+ *   dw[c][u][s]  = sum_{b,y,x} dout[y][x][c] v[y + u - pad][x + s - pad][c]
+ *   db[c]        = sum_{b,y,x} dout[y][x][c]
+ * (terms whose position falls outside the image are absent). dq, dk, dv are
+ * [B, H, W, C]; dw [C, ks, ks]; db [C] or NULL. All outputs are overwritten.
+ */
+int oracle_attend_backward(const double *q, const double *k, const double *v,
+                           const int32_t *idx, int B, int H, int W, int C, int heads,
+                           int S, int topk, const double *w, int ks, const double *dout,
+                           double *dq, double *dk, double *dv, double *dw, double *db) {
+  geom g;
+  if (!w || !dout || !dq || !dk || !dv || !dw ||
+      !attn_args_ok(q, k, v, idx, B, H, W, C, heads, S, topk, &g))
+    return ORACLE_EINVAL;
+  if (ks <= 0 || ks % 2 == 0) return ORACLE_EINVAL;
+  size_t total = (size_t)B * H * W * C;
+  memset(dq, 0, total * sizeof(double));
+  memset(dk, 0, total * sizeof(double));
+  memset(dv, 0, total * sizeof(double));
+  memset(dw, 0, (size_t)C * ks * ks * sizeof(double));
+  if (db) memset(db, 0, (size_t)C * sizeof(double));
+  attn_job J = {q, k, v, idx, g, heads, topk, NULL, 0};
+  int d = C / heads, nk = topk * g.n;
+  double scale = 1.0 / sqrt((double)d);
+  double *logit = malloc((size_t)nk * sizeof(double));
+  double *probs = malloc((size_t)nk * sizeof(double));
+  int32_t *keys = malloc((size_t)nk * sizeof(int32_t));
+  double *o = malloc((size_t)d * sizeof(double));
+  int rc = (logit && probs && keys && o) ? ORACLE_OK : ORACLE_EINVAL;
+  for (int b = 0; b < B && !rc; ++b)
+    for (int i = 0; i < g.R && !rc; ++i)
+      for (int t = 0; t < g.n && !rc; ++t)
+        for (int h = 0; h < heads && !rc; ++h) {
+          rc = attend_one(&J, b, i, t, h, logit, probs, keys, o);
+          if (rc) break;
+          int y, x;
+          region_token(&g, i, t, &y, &x);
+          size_t qo = offset_of(&g, b, y, x) + (size_t)h * d;
+          const double *go = dout + qo;
+          double D = 0.0;
+          for (int e = 0; e < d; ++e) D += go[e] * o[e];
+          for (int a = 0; a < nk; ++a) {
+            size_t ko = ((size_t)b * H * W + keys[a]) * C + (size_t)h * d;
+            double dp = 0.0;
+            for (int e = 0; e < d; ++e) dp += go[e] * v[ko + e];
+            double ds = probs[a] * (dp - D);
+            for (int e = 0; e < d; ++e) {
+              dv[ko + e] += probs[a] * go[e];
+              dq[qo + e] += scale * ds * k[ko + e];
+              dk[ko + e] += scale * ds * q[qo + e];
+            }
+          }
+        }
+  free(logit);
+  free(probs);
+  free(keys);
+  free(o);
+  if (rc) return rc;
+  int pad = ks / 2;
+  for (int b = 0; b < B; ++b)
+    for (int y = 0; y < H; ++y)
+      for (int x = 0; x < W; ++x)
+        for (int c = 0; c < C; ++c) {
+          double go = dout[(((size_t)b * H + y) * W + x) * C + c];
+          if (db) db[c] += go;
+          for (int u = 0; u < ks; ++u)
+            for (int s2 = 0; s2 < ks; ++s2) {
+              int yy = y + u - pad, xx = x + s2 - pad;
+              if (yy < 0 || yy >= H || xx < 0 || xx >= W) continue;
+              size_t vo = (((size_t)b * H + yy) * W + xx) * C + c;
+              dw[((size_t)c * ks + u) * ks + s2] += go * v[vo];
+              dv[vo] += w[((size_t)c * ks + u) * ks + s2] * go;
+            }
+        }
   return ORACLE_OK;
 }

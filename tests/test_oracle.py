@@ -475,3 +475,75 @@ def test_block_ffn_composes_the_stages():
     ty = tx + F.linear(F.gelu(tc), torch.from_numpy(w2), torch.from_numpy(b2))
     np.testing.assert_allclose(hc, tc.numpy(), atol=1e-12)
     np.testing.assert_allclose(y, ty.numpy(), atol=1e-12)
+
+
+# ---- the backward of attend (routing held fixed) ----------------------------
+
+def _torch_attend(q, k, v, idx, heads, S, w, bias):
+    """attend written with torch tensor ops (region reshape, gather of the
+    routed regions, one softmax per query over all routed keys, depthwise
+    conv2d for the LePE): an implementation independent of the oracle's loops,
+    differentiated by torch autograd in float64."""
+    B, H, W, C = q.shape
+    hr, wr, R, d = H // S, W // S, S * S, C // heads
+    n, topk = hr * wr, idx.shape[-1]
+
+    def regions(x):  # [B, R, n, C], regions and their tokens row-major
+        return x.reshape(B, S, hr, S, wr, C).permute(0, 1, 3, 2, 4, 5).reshape(B, R, n, C)
+
+    qr, kr, vr = regions(q), regions(k), regions(v)
+    ib = torch.from_numpy(np.asarray(idx, np.int64))
+    bi = torch.arange(B)[:, None, None]
+    kg = kr[bi, ib].reshape(B, R, topk * n, heads, d).permute(0, 3, 1, 2, 4)
+    vg = vr[bi, ib].reshape(B, R, topk * n, heads, d).permute(0, 3, 1, 2, 4)
+    qh = qr.reshape(B, R, n, heads, d).permute(0, 3, 1, 2, 4)
+    att = torch.softmax(qh @ kg.transpose(-1, -2) / math.sqrt(d), dim=-1)
+    o = (att @ vg).permute(0, 2, 3, 1, 4).reshape(B, S, S, hr, wr, C)
+    o = o.permute(0, 1, 3, 2, 4, 5).reshape(B, H, W, C)
+    lepe = torch.nn.functional.conv2d(v.permute(0, 3, 1, 2), w[:, None], bias,
+                                      padding=w.shape[-1] // 2, groups=C)
+    return o + lepe.permute(0, 2, 3, 1)
+
+
+@pytest.mark.parametrize("B,H,W,C,heads,S,topk,ks", [
+    (2, 8, 8, 8, 2, 2, 2, 3),     # 4 regions of 16 tokens, top-2
+    (1, 6, 9, 12, 3, 3, 4, 5),    # ragged 2 x 3 regions, 3 heads of 4
+    (1, 4, 4, 4, 1, 4, 16, 1),    # one-token regions, every region routed
+])
+def test_attend_backward_matches_torch_autograd(B, H, W, C, heads, S, topk, ks):
+    rng = np.random.default_rng(B * 100 + H + C + ks)
+    q, k, v = (rng.standard_normal((B, H, W, C)) for _ in range(3))
+    w = rng.standard_normal((C, ks, ks)) * 0.3
+    bias = rng.standard_normal(C) * 0.1
+    dout = rng.standard_normal((B, H, W, C))
+    idx, _ = oracle.route(q, k, S, topk)
+    dq, dk, dv, dw, db = oracle.attend_backward(q, k, v, idx, heads, S, w, dout)
+    t = [torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v, w, bias)]
+    out = _torch_attend(*t[:3], idx, heads, S, t[3], t[4])
+    assert np.allclose(out.detach().numpy(), oracle.attend(q, k, v, idx, heads, S, w, bias),
+                       atol=1e-12)
+    out.backward(torch.from_numpy(dout))
+    for got, ref in zip((dq, dk, dv, dw, db), t):
+        np.testing.assert_allclose(got, ref.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_attend_backward_is_the_derivative_of_attend():
+    """Central differences of L = sum(dout * attend(...)) along random
+    directions equal the oracle's gradients dotted with those directions."""
+    rng = np.random.default_rng(7)
+    B, H, W, C, heads, S, topk, ks = 1, 6, 6, 4, 2, 3, 3, 3
+    q, k, v = (rng.standard_normal((B, H, W, C)) for _ in range(3))
+    w, bias = rng.standard_normal((C, ks, ks)) * 0.3, rng.standard_normal(C) * 0.1
+    dout = rng.standard_normal((B, H, W, C))
+    idx, _ = oracle.route(q, k, S, topk)  # held fixed, as in the backward
+    grads = oracle.attend_backward(q, k, v, idx, heads, S, w, dout)
+    params = [q, k, v, w, bias]
+    L = lambda p: float(np.sum(dout * oracle.attend(*p[:3], idx, heads, S, p[3], p[4])))  # noqa: E731
+    for trial in range(4):
+        dirs = [rng.standard_normal(p.shape) for p in params]
+        eps = 1e-5
+        plus = [p + eps * d for p, d in zip(params, dirs)]
+        minus = [p - eps * d for p, d in zip(params, dirs)]
+        fd = (L(plus) - L(minus)) / (2 * eps)
+        an = sum(float(np.sum(g * d)) for g, d in zip(grads, dirs))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (trial, fd, an)
