@@ -245,6 +245,38 @@ int bra_linear(const void *x, const void *w, const float *bias, long long M, int
 int bra_dwconv_gelu(const void *h, const float *w, const float *bias, int B, int H, int W,
                     int Ch, int dtype, void *y, void *stream);
 
+/*
+ * bra_attend_backward -- the gradients of bra_attend's output (routed
+ * attention + LePE) with the routing held fixed: TopkRouting with
+ * diff_routing=False (the snabindia page §4) passes no gradient to the
+ * routing, so idx is a constant. Given dout = dL/dout, with P a query's
+ * softmax over its k*n routed keys, O its attention output, D = dout . O and
+ * scale = (C/heads)^-1/2:
+ *   dv[key] += P dout;  dS = P (dout . v[key] - D);
+ *   dq += scale dS k[key];  dk[key] += scale dS q;
+ *   dv += the LePE's transpose applied to dout;
+ *   dlepe_w[c][u][s] = sum_{b,y,x} dout[y][x][c] v[y+u-ks/2][x+s-ks/2][c];
+ *   dlepe_b[c] = sum_{b,y,x} dout[y][x][c].
+ *   q, k, v, dout  [B, H, W, C] device, dtype; idx, heads, S, topk, lepe_w,
+ *                  lepe_ks as bra_attend (the forward's bias does not enter)
+ *   dq, dk, dv     out: float32 [B, H, W, C] device, overwritten
+ *   dlepe_w        out: float32 [C, lepe_ks, lepe_ks] device, overwritten
+ *   dlepe_b        out (optional, may be NULL): float32 [C] device
+ * Arithmetic is float32; dk, dv and the LePE gradients are summed with
+ * atomic adds, so their last bits may differ from run to run. An index out
+ * of range reads zero keys (as bra_attend does), sends them no gradient and
+ * sets the device status word. Supported: C / heads <= 64, C <= 1024 and a
+ * per-block shared-memory footprint of 4 (2 n + 2 topk n)(C / heads + 1) +
+ * 4 n (topk n + 1) bytes within the limit (n = tokens per region);
+ * otherwise BRA_ERR_UNSUPPORTED. Outputs must not overlap the inputs or one
+ * another.
+ */
+int bra_attend_backward(const void *q, const void *k, const void *v, const int32_t *idx,
+                        int B, int H, int W, int C, int heads, int S, int topk,
+                        const float *lepe_w, int lepe_ks, const void *dout, int dtype,
+                        float *dq, float *dk, float *dv, float *dlepe_w, float *dlepe_b,
+                        void *stream);
+
 /* Bytes of the workspace bra_block_ffn needs; 0 on invalid sizes. */
 size_t bra_block_ffn_workspace_bytes(int B, int H, int W, int C);
 

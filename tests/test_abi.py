@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.bra_abi_version() == 102
+    assert lib.bra_abi_version() == 103
     assert bra.status_string(0) == "ok"
     assert "unsupported" in bra.status_string(2)
     assert bra.status_string(99) == "unknown status"
@@ -135,3 +135,27 @@ def test_projection_argument_errors(lib):
     assert f(A, B_, NULL, 100, 512, 1, C_, D_, G, NULL) == bra.BRA_ERR_UNSUPPORTED
     assert f(A, B_, NULL, 100, 64, 0, C_, D_, E_, NULL) == bra.BRA_ERR_UNSUPPORTED  # f32
     assert f(NULL, NULL, NULL, 0, 64, 1, NULL, NULL, NULL, NULL) == bra.BRA_OK  # empty
+
+
+G1, G2, G3, G4, G5 = (ctypes.c_void_p(0x90000000 + 0x08000000 * i) for i in range(5))
+
+
+def attend_backward(lib, q=A, k=B_, v=C_, idx=D_, B=1, H=14, W=14, C=64, heads=2, S=7,
+                    topk=4, w=E_, ks=5, dout=F_, dtype=1, dq=G1, dk=G2, dv=G3, dw=G4, db=G5):
+    return lib.bra_attend_backward(q, k, v, idx, B, H, W, C, heads, S, topk, w, ks, dout,
+                                   dtype, dq, dk, dv, dw, db, NULL)
+
+
+def test_attend_backward_argument_errors(lib):
+    assert attend_backward(lib, dout=NULL) == bra.BRA_ERR_INVALID_ARG
+    assert attend_backward(lib, dw=NULL) == bra.BRA_ERR_INVALID_ARG
+    assert attend_backward(lib, heads=3) == bra.BRA_ERR_INVALID_ARG   # C % heads
+    assert attend_backward(lib, ks=4) == bra.BRA_ERR_INVALID_ARG      # even kernel
+    assert attend_backward(lib, H=15) == bra.BRA_ERR_INVALID_ARG      # H % S
+    assert attend_backward(lib, dq=A) == bra.BRA_ERR_INVALID_ARG      # dq aliases q
+    assert attend_backward(lib, dk=G1) == bra.BRA_ERR_INVALID_ARG     # dk aliases dq
+    assert attend_backward(lib, db=G4) == bra.BRA_ERR_INVALID_ARG     # db aliases dw
+    assert attend_backward(lib, ks=9) == bra.BRA_ERR_UNSUPPORTED
+    assert attend_backward(lib, C=256, heads=2) == bra.BRA_ERR_UNSUPPORTED  # d = 128 > 64
+    assert attend_backward(lib, B=0, q=NULL, k=NULL, v=NULL, idx=NULL, w=NULL, dout=NULL,
+                           dq=NULL, dk=NULL, dv=NULL, dw=NULL, db=NULL) == bra.BRA_OK

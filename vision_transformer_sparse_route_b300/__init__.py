@@ -14,7 +14,7 @@ import os
 
 import torch
 
-__all__ = ["BraError", "qkv_project", "route", "attend", "attend_tc", "forward", "forward_static", "forward_host",
+__all__ = ["BraError", "qkv_project", "route", "attend", "attend_backward", "attend_tc", "forward", "forward_static", "forward_host",
            "HostPipeline",
            "idx_workspace_bytes", "forward_launches", "device_status", "check_wait_timeout", "library_path",
            "SYMBOLS"]
@@ -50,6 +50,8 @@ SYMBOLS = {
                            _I, _P, _P, _P]),
     "bra_block_attention": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I, _I, _I, _I, _I,
                                  _I, _P, _P, _I, _I, _P, _P, _P]),
+    "bra_attend_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _I,
+                                 _P, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -153,6 +155,21 @@ def attend(q, k, v, idx, heads: int, S: int, lepe_w, lepe_b=None, out=None, stre
                             _dtype_code(q), _ptr(out), _stream(stream))
     _check(rc, "bra_attend")
     return out
+
+
+def attend_backward(q, k, v, idx, heads: int, S: int, lepe_w, dout, stream=None):
+    """Gradients of attend's output for the upstream gradient dout, the
+    routing fixed: (dq, dk, dv, dlepe_w, dlepe_b), float32."""
+    B, H, W, C = _map(q, "q")
+    dq, dk, dv = (torch.empty(q.shape, dtype=torch.float32, device=q.device) for _ in range(3))
+    dw = torch.empty(lepe_w.shape, dtype=torch.float32, device=q.device)
+    db = torch.empty(C, dtype=torch.float32, device=q.device)
+    rc = _load().bra_attend_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(idx), B, H, W, C, heads,
+                                     S, idx.shape[-1], _ptr(lepe_w), lepe_w.shape[-1],
+                                     _ptr(dout), _dtype_code(q), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     _ptr(dw), _ptr(db), _stream(stream))
+    _check(rc, "bra_attend_backward")
+    return dq, dk, dv, dw, db
 
 
 def qkv_project(x, w, bias=None, q=None, k=None, v=None, stream=None):

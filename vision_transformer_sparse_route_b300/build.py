@@ -15,7 +15,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 SOURCES = ["bra.cu"]
 DEPS = ["bra.cu", "ptx.cuh", "route.cuh", "attend_bf16.cuh", "attend_f32.cuh", "per_device.h",
         "attend_image.cuh", "attend_tc.cuh", "tcgen05.cuh", "forward_image.cuh", "qkv_tc.cuh",
-        "block.cuh"]
+        "block.cuh", "backward.cuh"]
 
 
 def nvcc_command(out: str, extra: list[str] | None = None) -> list[str]:

@@ -18,6 +18,7 @@
 #include "attend_f32.cuh"
 #include "attend_image.cuh"
 #include "attend_tc.cuh"
+#include "backward.cuh"
 #include "block.cuh"
 #include "qkv_tc.cuh"
 #include "forward_image.cuh"
@@ -1484,6 +1485,111 @@ int bra_block_attention(const void *x, const float *ln_w, const float *ln_b, flo
   return bra_residual_add(x, y, (long long)mc, dtype, y, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shared memory of the attention backward: the region's Q and dout, the
+// routed keys' K and V (rows of d + 1 floats), P ([n][nk + 1]), D and the
+// token lists.
+bool plan_attend_bwd(int H, int W, int C, int heads, int S, int topk, bra::BwdGeom *g,
+                     size_t *smem) {
+  if (heads <= 0 || C % heads || C / heads > 64) return false;
+  bra::BwdGeom a = {};
+  a.H = H; a.W = W; a.C = C; a.S = S; a.heads = heads; a.topk = topk;
+  a.hr = H / S; a.wr = W / S; a.n = a.hr * a.wr; a.R = S * S; a.d = C / heads;
+  a.nk = topk * a.n;
+  a.ds = a.d + 1;
+  a.ps = a.nk + 1;
+  a.scale = (float)(1.0 / std::sqrt((double)a.d));
+  size_t off = (size_t)a.n * a.ds * 4;
+  a.off_do = (uint32_t)off; off += (size_t)a.n * a.ds * 4;
+  a.off_k = (uint32_t)off; off += (size_t)a.nk * a.ds * 4;
+  a.off_v = (uint32_t)off; off += (size_t)a.nk * a.ds * 4;
+  a.off_p = (uint32_t)off; off += (size_t)a.n * a.ps * 4;
+  a.off_d = (uint32_t)off; off += (size_t)a.n * 4;
+  a.off_tok = (uint32_t)round_up(off, 16); off = a.off_tok + (size_t)(a.nk + a.n) * 4;
+  *g = a;
+  *smem = off;
+  return off <= kMaxSmemPerBlock;
+}
+
+template <typename T>
+int launch_attend_bwd(const void *q, const void *k, const void *v, const int32_t *idx, int B,
+                      const float *w, int ks, const void *dout, const bra::BwdGeom &g,
+                      size_t smem, float *dq, float *dk, float *dv, float *dw, float *db,
+                      cudaStream_t s) {
+  auto kern = bra::bra_attend_bwd_kernel<T>;
+  if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
+    return BRA_ERR_CUDA;
+  const unsigned grid = (unsigned)((size_t)B * g.R * g.heads);
+  kern<<<grid, bra::kBwdThreads, smem, s>>>(static_cast<const T *>(q), static_cast<const T *>(k),
+                                            static_cast<const T *>(v), idx,
+                                            static_cast<const T *>(dout), g, dq, dk, dv);
+  int rc = cuda_status(cudaGetLastError());
+  if (rc) return rc;
+  const unsigned rows = (unsigned)((size_t)B * g.H);
+  const T *vt = static_cast<const T *>(v), *gt = static_cast<const T *>(dout);
+  switch (ks) {
+    case 1: bra::bra_lepe_bwd_kernel<T, 1><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
+    case 3: bra::bra_lepe_bwd_kernel<T, 3><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
+    case 5: bra::bra_lepe_bwd_kernel<T, 5><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
+    default: bra::bra_lepe_bwd_kernel<T, 7><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+int bra_attend_backward(const void *q, const void *k, const void *v, const int32_t *idx,
+                        int B, int H, int W, int C, int heads, int S, int topk,
+                        const float *lepe_w, int lepe_ks, const void *dout, int dtype,
+                        float *dq, float *dk, float *dv, float *dlepe_w, float *dlepe_b,
+                        void *stream) {
+  int rc = check_map_args(B, H, W, C, S, topk, dtype);
+  if (rc) return rc;
+  if (heads <= 0 || C % heads) return BRA_ERR_INVALID_ARG;
+  if (lepe_ks <= 0 || lepe_ks % 2 == 0) return BRA_ERR_INVALID_ARG;
+  if (B == 0) return BRA_OK;
+  if (!q || !k || !v || !idx || !lepe_w || !dout || !dq || !dk || !dv || !dlepe_w)
+    return BRA_ERR_INVALID_ARG;
+  const size_t in_bytes = (size_t)B * H * W * C * elem_size(dtype);
+  const size_t g_bytes = (size_t)B * H * W * C * 4;
+  const size_t w_bytes = (size_t)C * lepe_ks * lepe_ks * 4;
+  const void *ins[] = {q, k, v, dout};
+  float *outs[] = {dq, dk, dv};
+  for (int a = 0; a < 3; ++a) {
+    float *o = outs[a];
+    for (const void *in : ins)
+      if (overlap(o, g_bytes, in, in_bytes)) return BRA_ERR_INVALID_ARG;
+    for (int a2 = a + 1; a2 < 3; ++a2)
+      if (overlap(o, g_bytes, outs[a2], g_bytes)) return BRA_ERR_INVALID_ARG;
+    if (overlap(o, g_bytes, dlepe_w, w_bytes)) return BRA_ERR_INVALID_ARG;
+    if (dlepe_b && overlap(o, g_bytes, dlepe_b, (size_t)C * 4)) return BRA_ERR_INVALID_ARG;
+  }
+  if (dlepe_b && overlap(dlepe_w, w_bytes, dlepe_b, (size_t)C * 4)) return BRA_ERR_INVALID_ARG;
+  if (!lepe_ks_supported(lepe_ks) || C > 1024) return BRA_ERR_UNSUPPORTED;
+  if ((size_t)B * S * S * heads > 0x7fffffffu) return BRA_ERR_UNSUPPORTED;
+  bra::BwdGeom g;
+  size_t smem;
+  if (!plan_attend_bwd(H, W, C, heads, S, topk, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+  (void)cudaGetLastError();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // dq is written whole; the others are sums
+  if (cudaMemsetAsync(dk, 0, g_bytes, s) != cudaSuccess ||
+      cudaMemsetAsync(dv, 0, g_bytes, s) != cudaSuccess ||
+      cudaMemsetAsync(dlepe_w, 0, w_bytes, s) != cudaSuccess ||
+      (dlepe_b && cudaMemsetAsync(dlepe_b, 0, (size_t)C * 4, s) != cudaSuccess))
+    return BRA_ERR_CUDA;
+  if (dtype == BRA_F32)
+    return launch_attend_bwd<float>(q, k, v, idx, B, lepe_w, lepe_ks, dout, g, smem, dq, dk,
+                                    dv, dlepe_w, dlepe_b, s);
+  return launch_attend_bwd<__nv_bfloat16>(q, k, v, idx, B, lepe_w, lepe_ks, dout, g, smem, dq,
+                                          dk, dv, dlepe_w, dlepe_b, s);
+}
+
 size_t bra_idx_workspace_bytes(int B, int S, int topk) {
   if (B < 0 || S <= 0 || topk <= 0) return 0;
   return (size_t)B * S * S * topk * sizeof(int32_t);
@@ -1516,7 +1622,7 @@ const char *bra_status_string(int status) {
   }
 }
 
-int bra_abi_version(void) { return 102; }
+int bra_abi_version(void) { return 103; }
 
 int bra_check_wait_timeout(uint64_t limit_ns, void *stream) {
   if (limit_ns < 1000 || limit_ns > 1000000000ull) return BRA_ERR_INVALID_ARG;
