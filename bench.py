@@ -182,6 +182,25 @@ def ffn_work(wl: bra_synth.Workload) -> dict:
             "tensor_flops": 2 * 6 * M * C * C, "alu_flops": 2 * 9 * 3 * M * C, "exps": 0}
 
 
+def backward_work(wl: bra_synth.Workload) -> dict:
+    """Algorithmic work of the backward of attend (the routing fixed): q, k,
+    v and dout read once and dq, dk, dv written once (float32), the LePE
+    weights; the six contractions of the attention's backward (the logits and
+    O again, dout v^T, P^T dout, dS k and dS^T q: 2 k n d each per query and
+    head), on the tensor pipe for bf16 and the FMA pipe for float32; the
+    LePE's input and weight gradients (2 ks^2 each per element); one
+    exponential per query, routed key and head."""
+    e = 4 if wl.dtype == "f32" else 2
+    T = wl.B * wl.H * wl.W * wl.C
+    nk = wl.topk * wl.n
+    contraction = 6 * 2 * (wl.B * wl.H * wl.W) * nk * wl.C
+    lepe = 4 * wl.ks * wl.ks * T
+    return {"bytes": 4 * T * e + 3 * T * 4 + 2 * wl.C * wl.ks * wl.ks * 4,
+            "tensor_flops": contraction if wl.dtype == "bf16" else 0,
+            "alu_flops": lepe + (contraction if wl.dtype == "f32" else 0),
+            "exps": wl.B * wl.H * wl.W * wl.heads * nk}
+
+
 def peaks(sm_count: int | None = None, sm_mhz: float | None = None) -> dict:
     """Roofline denominators: HBM GB/s and bf16 tensor TFLOP/s measured on
     the B300s (MEASURED_PEAKS.json, burst figures for kernels timed
@@ -625,6 +644,65 @@ def time_block_ffn(wl, dev, stream, steps: int) -> float:
     return ms
 
 
+def time_backward(wl, dev, stream, steps: int) -> float:
+    """ms per bra_attend_backward call (the gradients of attend for a given
+    dout, the routing fixed) on the workload, from CUDA graphs over rotating
+    input sets larger than L2."""
+    import numpy as np
+    import torch
+    import vision_transformer_sparse_route_b300 as bra
+    x = bra_synth.make_inputs(wl, seed=0)
+    cast = (lambda a: torch.from_numpy(a).to(torch.bfloat16)) if wl.dtype == "bf16" else \
+        (lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)))
+    q, k, v = (cast(a).to(dev) for a in (x.q, x.k, x.v))
+    w = torch.from_numpy(x.lepe_w).to(dev)
+    rng = np.random.default_rng(5)
+    dout = cast(rng.standard_normal((wl.B, wl.H, wl.W, wl.C)).astype(np.float32)).to(dev)
+    idx = bra.route(q, k, wl.S, wl.topk)
+    e = 4 if wl.dtype == "f32" else 2
+    T = wl.B * wl.H * wl.W * wl.C
+    per_set = 4 * T * e + 3 * T * 4
+    sets = max(2, -(-3 * L2_BYTES // per_set) + 1)
+    bufs = [(q.clone(), k.clone(), v.clone(), dout.clone()) + tuple(
+        torch.empty((wl.B, wl.H, wl.W, wl.C), dtype=torch.float32, device=dev) for _ in range(3))
+        for _ in range(sets)]
+    dw = torch.empty(x.lepe_w.shape, dtype=torch.float32, device=dev)
+    db = torch.empty(wl.C, dtype=torch.float32, device=dev)
+    lib = bra._load()
+    code = bra.BRA_BF16 if wl.dtype == "bf16" else bra.BRA_F32
+
+    def call(qs, ks, vs, gs, dq, dk, dv):
+        rc = lib.bra_attend_backward(qs.data_ptr(), ks.data_ptr(), vs.data_ptr(), idx.data_ptr(),
+                                     wl.B, wl.H, wl.W, wl.C, wl.heads, wl.S, wl.topk,
+                                     w.data_ptr(), wl.ks, gs.data_ptr(), code, dq.data_ptr(),
+                                     dk.data_ptr(), dv.data_ptr(), dw.data_ptr(), db.data_ptr(),
+                                     stream.cuda_stream)
+        if rc != bra.BRA_OK:
+            raise RuntimeError(f"bra_attend_backward: {rc}")
+    graphs = []
+    with torch.cuda.stream(stream):
+        for t in bufs:
+            call(*t)
+        stream.synchronize()
+        for t in bufs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(*t)
+            graphs.append(g)
+        for i in range(3):
+            graphs[i % sets].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % sets].replay()
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del graphs, bufs
+    torch.cuda.empty_cache()
+    return ms
+
+
 def launch_floor(torch, stream, reps: int = 2000) -> dict:
     """Replay cost of a CUDA graph holding one near-empty kernel (a
     one-element fill) and one holding two of them in a chain, back to back
@@ -683,6 +761,8 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
     if wl.dtype == "bf16" and wl.C in (64, 128):
         # the block's ConvFFN branch (its fc2 takes K = 3C up to 384)
         ffn_ms = time_block_ffn(wl, dev, stream, kernel_steps)
+    # the backward of attend (the routing fixed)
+    bwd_ms = time_backward(wl, dev, stream, max(10, kernel_steps // 4))
     work = algorithmic_work(wl)
     ok = st.bra.device_status(stream)
     launches = st.launches()
@@ -706,6 +786,8 @@ def measure_workload(wl, dev, stream, pk, kernel_steps: int, cpu_seconds: float,
              **({"block_ffn_us": ffn_ms * 1e3,
                  "block_ffn_roofline": roofline(ffn_work(wl), pk, wl.dtype, ffn_ms * 1e-3)}
                 if ffn_ms is not None else {}),
+             "backward_us": bwd_ms * 1e3,
+             "backward_roofline": roofline(backward_work(wl), pk, wl.dtype, bwd_ms * 1e-3),
              **({"attend_tc_us": tc_ms * 1e3,
                  "attend_tc_roofline": roofline(work["attend"], pk, wl.dtype, tc_ms * 1e-3)}
                 if tc_ms is not None else {}),

@@ -265,9 +265,9 @@ int bra_dwconv_gelu(const void *h, const float *w, const float *bias, int B, int
  * Arithmetic is float32; dk, dv and the LePE gradients are summed with
  * atomic adds, so their last bits may differ from run to run. An index out
  * of range reads zero keys (as bra_attend does), sends them no gradient and
- * sets the device status word. Supported: C / heads <= 64, C <= 1024 and a
- * per-block shared-memory footprint of 4 (2 n + 2 topk n)(C / heads + 1) +
- * 4 n (topk n + 1) bytes within the limit (n = tokens per region);
+ * sets the device status word. Supported: C / heads <= 64 and a
+ * per-block shared-memory footprint of about 4 (2 n + 2 topk n)(C / heads + 1)
+ * + 8 n (topk n + 1) bytes within the limit (n = tokens per region);
  * otherwise BRA_ERR_UNSUPPORTED. Outputs must not overlap the inputs or one
  * another.
  */

@@ -181,3 +181,17 @@ def test_ffn_work_counts_each_step_once():
     # LayerNorm 2, fc1 4, convolution + GELU 6, fc2 5 (M C elements, bf16)
     assert w["bytes"] == 17 * M * C * 2 + 2 * 3 * C * C * 2 + 10 * 3 * C * 4
     assert w["tensor_flops"] == 2 * (2 * M * C * 3 * C)
+
+
+def test_backward_work_counts():
+    wl = bra_synth.WORKLOADS["stage1_bf16"]
+    T = wl.B * wl.H * wl.W * wl.C
+    w = bench.backward_work(wl)
+    # q, k, v, dout bf16 in; dq, dk, dv float32 out; LePE weights in and out
+    assert w["bytes"] == 4 * T * 2 + 3 * T * 4 + 2 * wl.C * 25 * 4
+    # six contractions of 2 * (k n) * d per query and head: 2 * 64 * C per token each
+    assert w["tensor_flops"] == 6 * 2 * 64 * T
+    assert w["alu_flops"] == 4 * 25 * T
+    assert w["exps"] == wl.B * wl.H * wl.W * wl.heads * 64
+    f = bench.backward_work(bra_synth.WORKLOADS["tiny_f32"])
+    assert f["tensor_flops"] == 0 and f["alu_flops"] > 4 * 25 * 14 * 14 * 64

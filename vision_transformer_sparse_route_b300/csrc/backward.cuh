@@ -29,7 +29,7 @@ struct BwdGeom {
   int ds;         // row stride of the Q, dO, K and V tiles (d + 1 floats)
   int ps;         // row stride of P (nk + 1 floats)
   float scale;    // d^-1/2
-  uint32_t off_do, off_k, off_v, off_p, off_d, off_tok;  // bytes into shared memory
+  uint32_t off_do, off_k, off_v, off_p, off_g, off_d, off_tok;  // bytes into shared memory
 };
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);
@@ -38,11 +38,55 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
   return __bfloat162float(x);
 }
 
+// out[i][j] = sum_r a[i * as_i + r * as_r] b[j * bs_j + r * bs_r] for i < M,
+// j < N over shared-memory operands, all threads of the CTA: each thread
+// computes 4 x 4 blocks of out in registers (eight loads feed sixteen FMAs)
+// and hands each element to consume(i, j, value).
+template <typename F>
+__device__ __forceinline__ void smem_gemm4x4(const float *a, int as_i, int as_r, const float *b,
+                                             int bs_j, int bs_r, int M, int N, int R, int tid,
+                                             F &&consume) {
+  const int tm = (M + 3) / 4, tn = (N + 3) / 4;
+  for (int e = tid; e < tm * tn; e += kBwdThreads) {
+    const int i0 = (e / tn) * 4, j0 = (e % tn) * 4;
+    int ia[4], jb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      ia[u] = min(i0 + u, M - 1) * as_i;
+      jb[u] = min(j0 + u, N - 1) * bs_j;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) acc[u][w] = 0.f;
+    for (int r = 0; r < R; ++r) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        av[u] = a[ia[u] + r * as_r];
+        bv[u] = b[jb[u] + r * bs_r];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(av[u], bv[w], acc[u][w]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        if (i0 + u < M && j0 + w < N) consume(i0 + u, j0 + w, acc[u][w]);
+  }
+}
+
 // One CTA per (image b, query region i, head h): the region's Q and dout, the
-// routed keys' K and V (float32, padded rows), P recomputed (the scaled
-// logits, then one softmax per query over all routed keys), then dv and dk
-// (atomic adds, one per key and channel) and dq (plain stores: a query
-// belongs to one region). Out-of-range routing reads zero keys, as the
+// routed keys' K and V (float32, padded rows), then, each contraction by
+// smem_gemm4x4: the scaled logits and one softmax per query over all routed
+// keys (P); dP = dout V^T; D = sum_key P dP (which is dout . O); dv = P^T dout
+// (atomic adds, one per key and channel); dS = P (dP - D) in dP's place;
+// dq = scale dS K (plain stores: a query belongs to one region) and dk =
+// scale dS^T Q (atomic adds). Out-of-range routing reads zero keys, as the
 // forward does, sets the status word and sends no gradient to them.
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads)
@@ -55,14 +99,15 @@ __global__ void __launch_bounds__(kBwdThreads)
   float *sdo = reinterpret_cast<float *>(bwd_smem + g.off_do);     // [n][ds]
   float *sk = reinterpret_cast<float *>(bwd_smem + g.off_k);       // [nk][ds]
   float *sv = reinterpret_cast<float *>(bwd_smem + g.off_v);       // [nk][ds]
-  float *sp = reinterpret_cast<float *>(bwd_smem + g.off_p);       // [n][ps]
+  float *sp = reinterpret_cast<float *>(bwd_smem + g.off_p);       // [n][ps]: P
+  float *sg = reinterpret_cast<float *>(bwd_smem + g.off_g);       // [n][ps]: dP, then dS
   float *sd = reinterpret_cast<float *>(bwd_smem + g.off_d);       // [n]
   int *ktok = reinterpret_cast<int *>(bwd_smem + g.off_tok);       // [nk], -1: none
   int *qtok = ktok + g.nk;                                         // [n]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x % g.heads, i = (blockIdx.x / g.heads) % g.R;
   const int b = blockIdx.x / (g.heads * g.R);
-  const int n = g.n, nk = g.nk, d = g.d;
+  const int n = g.n, nk = g.nk, d = g.d, ds = g.ds, ps = g.ps;
   const size_t img = (size_t)b * g.H * g.W;
 
   // token of every query and key (image-relative), -1 for out-of-range keys
@@ -86,8 +131,8 @@ __global__ void __launch_bounds__(kBwdThreads)
   for (int e = tid; e < n * d; e += kBwdThreads) {
     const int t = e / d, c = e - t * d;
     const size_t o = (img + qtok[t]) * g.C + h * d + c;
-    sq[t * g.ds + c] = to_f32(q[o]);
-    sdo[t * g.ds + c] = to_f32(dout[o]);
+    sq[t * ds + c] = to_f32(q[o]);
+    sdo[t * ds + c] = to_f32(dout[o]);
   }
   for (int e = tid; e < nk * d; e += kBwdThreads) {
     const int a = e / d, c = e - a * d;
@@ -97,22 +142,20 @@ __global__ void __launch_bounds__(kBwdThreads)
       kv = to_f32(k[o]);
       vv = to_f32(v[o]);
     }
-    sk[a * g.ds + c] = kv;
-    sv[a * g.ds + c] = vv;
+    sk[a * ds + c] = kv;
+    sv[a * ds + c] = vv;
   }
   __syncthreads();
 
-  // scaled logits, one thread per (query, key)
-  for (int e = tid; e < n * nk; e += kBwdThreads) {
-    const int t = e / nk, a = e - t * nk;
-    float s = 0.f;
-    for (int c = 0; c < d; ++c) s = fmaf(sq[t * g.ds + c], sk[a * g.ds + c], s);
-    sp[t * g.ps + a] = s * g.scale;
-  }
+  // scaled logits S = scale Q K^T and dP = dout V^T ([n][nk] each)
+  smem_gemm4x4(sq, ds, 1, sk, ds, 1, n, nk, d, tid,
+               [&](int t, int a, float x) { sp[t * ps + a] = x * g.scale; });
+  smem_gemm4x4(sdo, ds, 1, sv, ds, 1, n, nk, d, tid,
+               [&](int t, int a, float x) { sg[t * ps + a] = x; });
   __syncthreads();
-  // softmax of each query's row (a warp a row), then O and D = dout . O
+  // softmax of each row of S (a warp a row), then D = sum_key P dP
   for (int t = warp; t < n; t += kBwdWarps) {
-    float *row = sp + t * g.ps;
+    float *row = sp + t * ps;
     float m = -INFINITY;
     for (int a = lane; a < nk; a += 32) m = fmaxf(m, row[a]);
 #pragma unroll
@@ -126,95 +169,105 @@ __global__ void __launch_bounds__(kBwdThreads)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     const float inv = 1.f / sum;
-    for (int a = lane; a < nk; a += 32) row[a] *= inv;
-    __syncwarp();
     float dd = 0.f;
-    for (int c = lane; c < d; c += 32) {
-      float o = 0.f;
-      for (int a = 0; a < nk; ++a) o = fmaf(row[a], sv[a * g.ds + c], o);
-      dd = fmaf(sdo[t * g.ds + c], o, dd);
+    for (int a = lane; a < nk; a += 32) {
+      const float p = row[a] * inv;
+      row[a] = p;
+      dd = fmaf(p, sg[t * ps + a], dd);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
     if (lane == 0) sd[t] = dd;
   }
   __syncthreads();
-  // dv[key] = sum_t P[t][key] dout[t], one thread per (key, channel)
-  for (int e = tid; e < nk * d; e += kBwdThreads) {
-    const int a = e / d, c = e - a * d;
-    if (ktok[a] < 0) continue;
-    float acc = 0.f;
-    for (int t = 0; t < n; ++t) acc = fmaf(sp[t * g.ps + a], sdo[t * g.ds + c], acc);
-    atomicAdd(dv + (img + ktok[a]) * g.C + h * d + c, acc);
-  }
-  __syncthreads();
-  // dS = P (dout . v[key] - D), in place of P, one thread per (query, key)
+  // dv = P^T dout ([nk][d], atomic); dS = P (dP - D) in dP's place
+  smem_gemm4x4(sp, 1, ps, sdo, 1, ds, nk, d, n, tid, [&](int a, int c, float x) {
+    if (ktok[a] >= 0) atomicAdd(dv + (img + ktok[a]) * g.C + h * d + c, x);
+  });
   for (int e = tid; e < n * nk; e += kBwdThreads) {
     const int t = e / nk, a = e - t * nk;
-    float dp = 0.f;
-    for (int c = 0; c < d; ++c) dp = fmaf(sdo[t * g.ds + c], sv[a * g.ds + c], dp);
-    sp[t * g.ps + a] = sp[t * g.ps + a] * (dp - sd[t]);
+    sg[t * ps + a] = sp[t * ps + a] * (sg[t * ps + a] - sd[t]);
   }
   __syncthreads();
-  // dq = scale dS k (each query once), dk = scale dS^T q (atomic)
-  for (int e = tid; e < n * d; e += kBwdThreads) {
-    const int t = e / d, c = e - t * d;
-    float acc = 0.f;
-    for (int a = 0; a < nk; ++a) acc = fmaf(sp[t * g.ps + a], sk[a * g.ds + c], acc);
-    dq[(img + qtok[t]) * g.C + h * d + c] = acc * g.scale;
-  }
-  for (int e = tid; e < nk * d; e += kBwdThreads) {
-    const int a = e / d, c = e - a * d;
-    if (ktok[a] < 0) continue;
-    float acc = 0.f;
-    for (int t = 0; t < n; ++t) acc = fmaf(sp[t * g.ps + a], sq[t * g.ds + c], acc);
-    atomicAdd(dk + (img + ktok[a]) * g.C + h * d + c, acc * g.scale);
-  }
+  // dq = scale dS K (each query once), dk = scale dS^T Q (atomic)
+  smem_gemm4x4(sg, ps, 1, sk, 1, ds, n, d, nk, tid, [&](int t, int c, float x) {
+    dq[(img + qtok[t]) * g.C + h * d + c] = x * g.scale;
+  });
+  smem_gemm4x4(sg, 1, ps, sq, 1, ds, nk, d, n, tid, [&](int a, int c, float x) {
+    if (ktok[a] >= 0) atomicAdd(dk + (img + ktok[a]) * g.C + h * d + c, x * g.scale);
+  });
 }
 
-// The LePE's part, one CTA per image row (b, y), one thread per channel:
-// dv[y][x][c] += sum_{u,s} w[c][u][s] dout[y-u+p][x-s+p][c] (a plain add:
-// this grid runs after the attention's and owns each element), and the row's
-// sums of dout[y][x][c] v[y+u-p][x+s-p][c] and of dout, added to dw and db.
+// The LePE's part, one CTA per image row (b, y): thread (c, xp) takes
+// channel c (c = threadIdx.x % C) at the row's columns x = xp, xp + XP, ...
+// (XP = blockDim.x / C): dv[y][x][c] += sum_{u,s} w[c][u][s]
+// dout[y-u+p][x-s+p][c] (a plain add: this grid runs after the attention's
+// and owns each element), and its sums of dout[y][x][c] v[y+u-p][x+s-p][c]
+// and of dout; the XP partial sums of a channel are added in shared memory,
+// then to dw and db. blockDim.x is a multiple of C (C <= NT) or NT with the
+// channels in turns of NT.
+template <int KS>
+__host__ __device__ constexpr int lepe_bwd_threads() {
+  return KS >= 7 ? 128 : kBwdThreads;  // the partial sums fit in static shared memory
+}
+
 template <typename T, int KS>
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(lepe_bwd_threads<KS>())
     bra_lepe_bwd_kernel(const T *__restrict__ v, const float *__restrict__ w,
                         const T *__restrict__ dout, int H, int W, int C,
                         float *__restrict__ dv, float *__restrict__ dw,
                         float *__restrict__ db) {
   constexpr int PAD = KS / 2;
-  const int c = threadIdx.x, y = blockIdx.x % H, b = blockIdx.x / H;
-  if (c >= C) return;
-  float wt[KS * KS], gw[KS * KS];
-#pragma unroll
-  for (int e = 0; e < KS * KS; ++e) {
-    wt[e] = __ldg(w + (size_t)c * KS * KS + e);
-    gw[e] = 0.f;
-  }
-  float gb = 0.f;
+  __shared__ float part[lepe_bwd_threads<KS>()][KS * KS + 1];
+  const int y = blockIdx.x % H, b = blockIdx.x / H;
   const size_t img = (size_t)b * H * W;
-  for (int x = 0; x < W; ++x) {
-    const float go = to_f32(dout[(img + (size_t)y * W + x) * C + c]);
-    gb += go;
-    float acc = 0.f;
+  const int cw = C < (int)blockDim.x ? C : (int)blockDim.x;  // channels a turn
+  const int XP = blockDim.x / cw, xp = threadIdx.x / cw;
+  for (int c0 = 0; c0 < C; c0 += cw) {
+    const int c = c0 + threadIdx.x % cw;
+    float wt[KS * KS], gw[KS * KS];
 #pragma unroll
-    for (int u = 0; u < KS; ++u) {
-      const int yy = y + u - PAD;  // input row of tap u for output (y, x)
-      const int yo = y - u + PAD;  // output row that reads (y, x) through tap u
+    for (int e = 0; e < KS * KS; ++e) {
+      wt[e] = c < C ? __ldg(w + (size_t)c * KS * KS + e) : 0.f;
+      gw[e] = 0.f;
+    }
+    float gb = 0.f;
+    for (int x = xp; x < W && c < C; x += XP) {
+      const float go = to_f32(dout[(img + (size_t)y * W + x) * C + c]);
+      gb += go;
+      float acc = 0.f;
 #pragma unroll
-      for (int s = 0; s < KS; ++s) {
-        const int xx = x + s - PAD, xo = x - s + PAD;
-        if (yy >= 0 && yy < H && xx >= 0 && xx < W)
-          gw[u * KS + s] = fmaf(go, to_f32(v[(img + (size_t)yy * W + xx) * C + c]), gw[u * KS + s]);
-        if (yo >= 0 && yo < H && xo >= 0 && xo < W)
-          acc = fmaf(wt[u * KS + s], to_f32(dout[(img + (size_t)yo * W + xo) * C + c]), acc);
+      for (int u = 0; u < KS; ++u) {
+        const int yy = y + u - PAD;  // input row of tap u for output (y, x)
+        const int yo = y - u + PAD;  // output row that reads (y, x) through tap u
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          const int xx = x + s - PAD, xo = x - s + PAD;
+          if (yy >= 0 && yy < H && xx >= 0 && xx < W)
+            gw[u * KS + s] =
+                fmaf(go, to_f32(v[(img + (size_t)yy * W + xx) * C + c]), gw[u * KS + s]);
+          if (yo >= 0 && yo < H && xo >= 0 && xo < W)
+            acc = fmaf(wt[u * KS + s], to_f32(dout[(img + (size_t)yo * W + xo) * C + c]), acc);
+        }
+      }
+      dv[(img + (size_t)y * W + x) * C + c] += acc;
+    }
+#pragma unroll
+    for (int e = 0; e < KS * KS; ++e) part[threadIdx.x][e] = gw[e];
+    part[threadIdx.x][KS * KS] = gb;
+    __syncthreads();
+    if (xp == 0 && c < C) {
+      for (int e = 0; e <= KS * KS; ++e) {
+        float a = part[threadIdx.x][e];
+        for (int o = 1; o < XP; ++o) a += part[threadIdx.x + o * cw][e];
+        if (e < KS * KS)
+          atomicAdd(dw + (size_t)c * KS * KS + e, a);
+        else if (db)
+          atomicAdd(db + c, a);
       }
     }
-    dv[(img + (size_t)y * W + x) * C + c] += acc;
+    __syncthreads();
   }
-#pragma unroll
-  for (int e = 0; e < KS * KS; ++e) atomicAdd(dw + (size_t)c * KS * KS + e, gw[e]);
-  if (db) atomicAdd(db + c, gb);
 }
 
 }  // namespace bra

@@ -1490,8 +1490,8 @@ int bra_block_attention(const void *x, const float *ln_w, const float *ln_b, flo
 namespace {
 
 // Shared memory of the attention backward: the region's Q and dout, the
-// routed keys' K and V (rows of d + 1 floats), P ([n][nk + 1]), D and the
-// token lists.
+// routed keys' K and V (rows of d + 1 floats), P and dP ([n][nk + 1] each),
+// D and the token lists.
 bool plan_attend_bwd(int H, int W, int C, int heads, int S, int topk, bra::BwdGeom *g,
                      size_t *smem) {
   if (heads <= 0 || C % heads || C / heads > 64) return false;
@@ -1507,6 +1507,7 @@ bool plan_attend_bwd(int H, int W, int C, int heads, int S, int topk, bra::BwdGe
   a.off_k = (uint32_t)off; off += (size_t)a.nk * a.ds * 4;
   a.off_v = (uint32_t)off; off += (size_t)a.nk * a.ds * 4;
   a.off_p = (uint32_t)off; off += (size_t)a.n * a.ps * 4;
+  a.off_g = (uint32_t)off; off += (size_t)a.n * a.ps * 4;
   a.off_d = (uint32_t)off; off += (size_t)a.n * 4;
   a.off_tok = (uint32_t)round_up(off, 16); off = a.off_tok + (size_t)(a.nk + a.n) * 4;
   *g = a;
@@ -1529,12 +1530,24 @@ int launch_attend_bwd(const void *q, const void *k, const void *v, const int32_t
   int rc = cuda_status(cudaGetLastError());
   if (rc) return rc;
   const unsigned rows = (unsigned)((size_t)B * g.H);
+  // a multiple of C threads (several columns of a row at once), or all of
+  // the kernel's threads with the channels in turns
+  const int NT = ks >= 7 ? bra::lepe_bwd_threads<7>() : bra::lepe_bwd_threads<5>();
+  const unsigned nt = (unsigned)(g.C <= NT ? (NT / g.C) * g.C : NT);
   const T *vt = static_cast<const T *>(v), *gt = static_cast<const T *>(dout);
   switch (ks) {
-    case 1: bra::bra_lepe_bwd_kernel<T, 1><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
-    case 3: bra::bra_lepe_bwd_kernel<T, 3><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
-    case 5: bra::bra_lepe_bwd_kernel<T, 5><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
-    default: bra::bra_lepe_bwd_kernel<T, 7><<<rows, g.C, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db); break;
+    case 1:
+      bra::bra_lepe_bwd_kernel<T, 1><<<rows, nt, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db);
+      break;
+    case 3:
+      bra::bra_lepe_bwd_kernel<T, 3><<<rows, nt, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db);
+      break;
+    case 5:
+      bra::bra_lepe_bwd_kernel<T, 5><<<rows, nt, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db);
+      break;
+    default:
+      bra::bra_lepe_bwd_kernel<T, 7><<<rows, nt, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db);
+      break;
   }
   return cuda_status(cudaGetLastError());
 }
@@ -1570,7 +1583,7 @@ int bra_attend_backward(const void *q, const void *k, const void *v, const int32
     if (dlepe_b && overlap(o, g_bytes, dlepe_b, (size_t)C * 4)) return BRA_ERR_INVALID_ARG;
   }
   if (dlepe_b && overlap(dlepe_w, w_bytes, dlepe_b, (size_t)C * 4)) return BRA_ERR_INVALID_ARG;
-  if (!lepe_ks_supported(lepe_ks) || C > 1024) return BRA_ERR_UNSUPPORTED;
+  if (!lepe_ks_supported(lepe_ks)) return BRA_ERR_UNSUPPORTED;
   if ((size_t)B * S * S * heads > 0x7fffffffu) return BRA_ERR_UNSUPPORTED;
   bra::BwdGeom g;
   size_t smem;
