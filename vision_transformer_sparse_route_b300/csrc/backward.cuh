@@ -29,6 +29,7 @@ struct BwdGeom {
   int ds;         // row stride of the Q, dO, K and V tiles (d + 1 floats)
   int ps;         // row stride of P (nk + 1 floats)
   float scale;    // d^-1/2
+  int vec4;       // d % 4 == 0 and dq, dk, dv 16-byte aligned: 16-byte stores and atomics
   uint32_t off_do, off_k, off_v, off_p, off_g, off_d, off_tok;  // bytes into shared memory
 };
 
@@ -41,7 +42,8 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 // out[i][j] = sum_r a[i * as_i + r * as_r] b[j * bs_j + r * bs_r] for i < M,
 // j < N over shared-memory operands, all threads of the CTA: each thread
 // computes 4 x 4 blocks of out in registers (eight loads feed sixteen FMAs)
-// and hands each element to consume(i, j, value).
+// and hands each row of a block to consume(i, j0, vals, count): out[i][j0 +
+// e] = vals[e] for e < count (count < 4 only at the right edge).
 template <typename F>
 __device__ __forceinline__ void smem_gemm4x4(const float *a, int as_i, int as_r, const float *b,
                                              int bs_j, int bs_r, int M, int N, int R, int tid,
@@ -72,11 +74,22 @@ __device__ __forceinline__ void smem_gemm4x4(const float *a, int as_i, int as_r,
 #pragma unroll
         for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(av[u], bv[w], acc[u][w]);
     }
+    const int count = min(4, N - j0);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int w = 0; w < 4; ++w)
-        if (i0 + u < M && j0 + w < N) consume(i0 + u, j0 + w, acc[u][w]);
+      if (i0 + u < M) consume(i0 + u, j0, acc[u], count);
+  }
+}
+
+// Adds vals[0 .. count-1] to dst[0 .. count-1]: one 16-byte vector atomic
+// when the four are there and vec4 (dst 16-byte aligned), else one a value.
+__device__ __forceinline__ void atomic_add_row(float *dst, const float (&vals)[4], int count,
+                                               float scale, bool vec4) {
+  if (vec4 && count == 4) {
+    atomicAdd(reinterpret_cast<float4 *>(dst),
+              make_float4(vals[0] * scale, vals[1] * scale, vals[2] * scale, vals[3] * scale));
+  } else {
+    for (int e = 0; e < count; ++e) atomicAdd(dst + e, vals[e] * scale);
   }
 }
 
@@ -149,9 +162,13 @@ __global__ void __launch_bounds__(kBwdThreads)
 
   // scaled logits S = scale Q K^T and dP = dout V^T ([n][nk] each)
   smem_gemm4x4(sq, ds, 1, sk, ds, 1, n, nk, d, tid,
-               [&](int t, int a, float x) { sp[t * ps + a] = x * g.scale; });
+               [&](int t, int a0, const float (&x)[4], int cnt) {
+                 for (int e = 0; e < cnt; ++e) sp[t * ps + a0 + e] = x[e] * g.scale;
+               });
   smem_gemm4x4(sdo, ds, 1, sv, ds, 1, n, nk, d, tid,
-               [&](int t, int a, float x) { sg[t * ps + a] = x; });
+               [&](int t, int a0, const float (&x)[4], int cnt) {
+                 for (int e = 0; e < cnt; ++e) sg[t * ps + a0 + e] = x[e];
+               });
   __syncthreads();
   // softmax of each row of S (a warp a row), then D = sum_key P dP
   for (int t = warp; t < n; t += kBwdWarps) {
@@ -181,21 +198,32 @@ __global__ void __launch_bounds__(kBwdThreads)
   }
   __syncthreads();
   // dv = P^T dout ([nk][d], atomic); dS = P (dP - D) in dP's place
-  smem_gemm4x4(sp, 1, ps, sdo, 1, ds, nk, d, n, tid, [&](int a, int c, float x) {
-    if (ktok[a] >= 0) atomicAdd(dv + (img + ktok[a]) * g.C + h * d + c, x);
-  });
+  smem_gemm4x4(sp, 1, ps, sdo, 1, ds, nk, d, n, tid,
+               [&](int a, int c0, const float (&x)[4], int cnt) {
+                 if (ktok[a] >= 0)
+                   atomic_add_row(dv + (img + ktok[a]) * g.C + h * d + c0, x, cnt, 1.f, g.vec4);
+               });
   for (int e = tid; e < n * nk; e += kBwdThreads) {
     const int t = e / nk, a = e - t * nk;
     sg[t * ps + a] = sp[t * ps + a] * (sg[t * ps + a] - sd[t]);
   }
   __syncthreads();
   // dq = scale dS K (each query once), dk = scale dS^T Q (atomic)
-  smem_gemm4x4(sg, ps, 1, sk, 1, ds, n, d, nk, tid, [&](int t, int c, float x) {
-    dq[(img + qtok[t]) * g.C + h * d + c] = x * g.scale;
-  });
-  smem_gemm4x4(sg, 1, ps, sq, 1, ds, nk, d, n, tid, [&](int a, int c, float x) {
-    if (ktok[a] >= 0) atomicAdd(dk + (img + ktok[a]) * g.C + h * d + c, x * g.scale);
-  });
+  smem_gemm4x4(sg, ps, 1, sk, 1, ds, n, d, nk, tid,
+               [&](int t, int c0, const float (&x)[4], int cnt) {
+                 float *dst = dq + (img + qtok[t]) * g.C + h * d + c0;
+                 if (g.vec4 && cnt == 4)
+                   *reinterpret_cast<float4 *>(dst) =
+                       make_float4(x[0] * g.scale, x[1] * g.scale, x[2] * g.scale, x[3] * g.scale);
+                 else
+                   for (int e = 0; e < cnt; ++e) dst[e] = x[e] * g.scale;
+               });
+  smem_gemm4x4(sg, 1, ps, sq, 1, ds, nk, d, n, tid,
+               [&](int a, int c0, const float (&x)[4], int cnt) {
+                 if (ktok[a] >= 0)
+                   atomic_add_row(dk + (img + ktok[a]) * g.C + h * d + c0, x, cnt, g.scale,
+                                  g.vec4);
+               });
 }
 
 // The LePE's part, one CTA per image row (b, y): thread (c, xp) takes
@@ -248,6 +276,89 @@ __global__ void __launch_bounds__(lepe_bwd_threads<KS>())
                 fmaf(go, to_f32(v[(img + (size_t)yy * W + xx) * C + c]), gw[u * KS + s]);
           if (yo >= 0 && yo < H && xo >= 0 && xo < W)
             acc = fmaf(wt[u * KS + s], to_f32(dout[(img + (size_t)yo * W + xo) * C + c]), acc);
+        }
+      }
+      dv[(img + (size_t)y * W + x) * C + c] += acc;
+    }
+#pragma unroll
+    for (int e = 0; e < KS * KS; ++e) part[threadIdx.x][e] = gw[e];
+    part[threadIdx.x][KS * KS] = gb;
+    __syncthreads();
+    if (xp == 0 && c < C) {
+      for (int e = 0; e <= KS * KS; ++e) {
+        float a = part[threadIdx.x][e];
+        for (int o = 1; o < XP; ++o) a += part[threadIdx.x + o * cw][e];
+        if (e < KS * KS)
+          atomicAdd(dw + (size_t)c * KS * KS + e, a);
+        else if (db)
+          atomicAdd(db + c, a);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// The same LePE backward with the rows it reads staged in shared memory: the
+// KS rows of dout and of v around row y (rows outside the image and the
+// ks/2 columns on each side are zero), as [KS][W + 2 pad][C] in the input's
+// type, then the taps as unconditional shared-memory reads. Same arithmetic
+// and order as bra_lepe_bwd_kernel.
+template <typename T, int KS>
+__global__ void __launch_bounds__(lepe_bwd_threads<KS>())
+    bra_lepe_bwd_staged_kernel(const T *__restrict__ v, const float *__restrict__ w,
+                               const T *__restrict__ dout, int H, int W, int C,
+                               float *__restrict__ dv, float *__restrict__ dw,
+                               float *__restrict__ db) {
+  constexpr int PAD = KS / 2;
+  constexpr int EPV = 16 / sizeof(T);  // elements a 16-byte vector
+  __shared__ float part[lepe_bwd_threads<KS>()][KS * KS + 1];
+  extern __shared__ __align__(16) uint8_t lepe_smem[];
+  const int WP = W + 2 * PAD;
+  T *sg = reinterpret_cast<T *>(lepe_smem);  // dout rows y-pad .. y+pad
+  T *sv = sg + (size_t)KS * WP * C;          // v rows y-pad .. y+pad
+  const int y = blockIdx.x % H, b = blockIdx.x / H;
+  const size_t img = (size_t)b * H * W;
+  // stage both windows, 16 bytes a thread at a time (C * sizeof(T) is a
+  // multiple of 16)
+  const int vecs = KS * WP * C / EPV;
+  for (int e = threadIdx.x; e < 2 * vecs; e += blockDim.x) {
+    const int which = e / vecs, r = e - which * vecs;
+    const int row = r / (WP * C / EPV), rest = r - row * (WP * C / EPV);
+    const int xs = rest / (C / EPV), cv = rest - xs * (C / EPV);
+    const int yy = y + row - PAD, xx = xs - PAD;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (yy >= 0 && yy < H && xx >= 0 && xx < W)
+      val = __ldg(reinterpret_cast<const uint4 *>((which ? v : dout) +
+                                                  (img + (size_t)yy * W + xx) * C) + cv);
+    reinterpret_cast<uint4 *>(which ? sv : sg)[r] = val;
+  }
+  __syncthreads();
+  const int cw = C < (int)blockDim.x ? C : (int)blockDim.x;  // channels a turn
+  const int XP = blockDim.x / cw, xp = threadIdx.x / cw;
+  for (int c0 = 0; c0 < C; c0 += cw) {
+    const int c = c0 + threadIdx.x % cw;
+    float wt[KS * KS], gw[KS * KS];
+#pragma unroll
+    for (int e = 0; e < KS * KS; ++e) {
+      wt[e] = c < C ? __ldg(w + (size_t)c * KS * KS + e) : 0.f;
+      gw[e] = 0.f;
+    }
+    float gb = 0.f;
+    for (int x = xp; x < W && c < C; x += XP) {
+      // window row u holds image row y + u - pad; column x + s of it holds
+      // image column x + s - pad
+      const float go = to_f32(sg[((size_t)PAD * WP + x + PAD) * C + c]);
+      gb += go;
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < KS; ++u) {
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          gw[u * KS + s] =
+              fmaf(go, to_f32(sv[((size_t)u * WP + x + s) * C + c]), gw[u * KS + s]);
+          // dout at (y - u + pad, x - s + pad): window row KS-1-u, column x + KS-1-s
+          acc = fmaf(wt[u * KS + s],
+                     to_f32(sg[((size_t)(KS - 1 - u) * WP + x + KS - 1 - s) * C + c]), acc);
         }
       }
       dv[(img + (size_t)y * W + x) * C + c] += acc;

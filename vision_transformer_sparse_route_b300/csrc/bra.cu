@@ -1535,6 +1535,41 @@ int launch_attend_bwd(const void *q, const void *k, const void *v, const int32_t
   const int NT = ks >= 7 ? bra::lepe_bwd_threads<7>() : bra::lepe_bwd_threads<5>();
   const unsigned nt = (unsigned)(g.C <= NT ? (NT / g.C) * g.C : NT);
   const T *vt = static_cast<const T *>(v), *gt = static_cast<const T *>(dout);
+  // the rows staged in shared memory when they fit (C * sizeof(T) a multiple
+  // of 16 bytes), else read from global memory
+  const size_t staged = (size_t)2 * ks * (g.W + ks - 1) * g.C * sizeof(T);
+  const size_t static_part = (size_t)NT * (ks * ks + 1) * 4;
+  if ((g.C * sizeof(T)) % 16 == 0 && aligned16(v) && aligned16(dout) &&
+      staged + static_part <= kMaxSmemPerBlock) {
+    const void *kern = ks == 1   ? reinterpret_cast<const void *>(bra::bra_lepe_bwd_staged_kernel<T, 1>)
+                       : ks == 3 ? reinterpret_cast<const void *>(bra::bra_lepe_bwd_staged_kernel<T, 3>)
+                       : ks == 5 ? reinterpret_cast<const void *>(bra::bra_lepe_bwd_staged_kernel<T, 5>)
+                                 : reinterpret_cast<const void *>(bra::bra_lepe_bwd_staged_kernel<T, 7>);
+    // the dynamic part's limit, beside the kernel's static partial sums
+    if (staged + static_part > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kMaxSmemPerBlock - static_part)) != cudaSuccess)
+      return BRA_ERR_CUDA;
+    switch (ks) {
+      case 1:
+        bra::bra_lepe_bwd_staged_kernel<T, 1><<<rows, nt, staged, s>>>(vt, w, gt, g.H, g.W, g.C,
+                                                                       dv, dw, db);
+        break;
+      case 3:
+        bra::bra_lepe_bwd_staged_kernel<T, 3><<<rows, nt, staged, s>>>(vt, w, gt, g.H, g.W, g.C,
+                                                                       dv, dw, db);
+        break;
+      case 5:
+        bra::bra_lepe_bwd_staged_kernel<T, 5><<<rows, nt, staged, s>>>(vt, w, gt, g.H, g.W, g.C,
+                                                                       dv, dw, db);
+        break;
+      default:
+        bra::bra_lepe_bwd_staged_kernel<T, 7><<<rows, nt, staged, s>>>(vt, w, gt, g.H, g.W, g.C,
+                                                                       dv, dw, db);
+        break;
+    }
+    return cuda_status(cudaGetLastError());
+  }
   switch (ks) {
     case 1:
       bra::bra_lepe_bwd_kernel<T, 1><<<rows, nt, 0, s>>>(vt, w, gt, g.H, g.W, g.C, dv, dw, db);
@@ -1588,6 +1623,7 @@ int bra_attend_backward(const void *q, const void *k, const void *v, const int32
   bra::BwdGeom g;
   size_t smem;
   if (!plan_attend_bwd(H, W, C, heads, S, topk, &g, &smem)) return BRA_ERR_UNSUPPORTED;
+  g.vec4 = g.d % 4 == 0 && aligned16(dq) && aligned16(dk) && aligned16(dv);
   (void)cudaGetLastError();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // dq is written whole; the others are sums
