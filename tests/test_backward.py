@@ -74,3 +74,30 @@ def test_attend_backward_rejects_wide_heads(cuda_device):
     idx = bra.route(q, k, wl.S, wl.topk)
     with pytest.raises(bra.BraError):
         bra.attend_backward(q, k, v, idx, wl.heads, wl.S, w, q)
+
+
+def test_attend_backward_out_of_range_index_flags_and_spares_other_regions(cuda_device):
+    """An out-of-range routing entry (in the last query region) sets the
+    status word and leaves every gradient finite; dq of a region whose own
+    routing is valid still equals the oracle's."""
+    wl = Workload("bwd_bad", 1, 8, 8, 64, 2, 2, 2, 3, "bf16")
+    x = bra_synth.make_inputs(wl, seed=4)
+    q, k, v, w, _ = device_inputs(wl, x, cuda_device)
+    R = wl.S * wl.S
+    good = np.stack([np.arange(R), (np.arange(R) + 1) % R], axis=1)[None].astype(np.int32)
+    bad = good.copy()
+    bad[0, R - 1, 1] = R + 3
+    dout = torch.from_numpy(np.random.default_rng(4).standard_normal(q.shape).astype(np.float32))
+    dout = dout.to(torch.bfloat16).to(cuda_device)
+    bra.device_status(clear=True)
+    grads = bra.attend_backward(q, k, v, torch.from_numpy(bad).to(cuda_device), wl.heads, wl.S,
+                                w, dout)
+    assert bra.device_status(clear=True) == bra.BRA_ERR_INVALID_ARG
+    assert bra.device_status(clear=True) == bra.BRA_OK
+    for g in grads:
+        assert torch.isfinite(g).all()
+    refs = oracle.attend_backward(f64(q), f64(k), f64(v), good, wl.heads, wl.S, x.lepe_w,
+                                  f64(dout))
+    hr = wl.H // wl.S
+    got_dq, ref_dq = grads[0][:, :hr, :hr], refs[0][:, :hr, :hr]  # region 0
+    assert close(got_dq, ref_dq)
