@@ -100,8 +100,10 @@ __device__ __forceinline__ void atomic_add_row(float *dst, const float (&vals)[4
 // (atomic adds, one per key and channel); dS = P (dP - D) in dP's place;
 // dq = scale dS K (plain stores: a query belongs to one region) and dk =
 // scale dS^T Q (atomic adds). Out-of-range routing reads zero keys, as the
-// forward does, sets the status word and sends no gradient to them.
-template <typename T>
+// forward does, sets the status word and sends no gradient to them. D and NK,
+// when not zero, fix the head dimension and the keys a query at compile time
+// (the strides and loop bounds of the contractions then fold).
+template <typename T, int D, int NK>
 __global__ void __launch_bounds__(kBwdThreads)
     bra_attend_bwd_kernel(const T *__restrict__ q, const T *__restrict__ k,
                           const T *__restrict__ v, const int32_t *__restrict__ idx,
@@ -120,7 +122,9 @@ __global__ void __launch_bounds__(kBwdThreads)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x % g.heads, i = (blockIdx.x / g.heads) % g.R;
   const int b = blockIdx.x / (g.heads * g.R);
-  const int n = g.n, nk = g.nk, d = g.d, ds = g.ds, ps = g.ps;
+  const int n = g.n;
+  const int nk = NK ? NK : g.nk, ps = NK ? NK + 1 : g.ps;
+  const int d = D ? D : g.d, ds = D ? D + 1 : g.ds;
   const size_t img = (size_t)b * g.H * g.W;
 
   // token of every query and key (image-relative), -1 for out-of-range keys

@@ -1520,7 +1520,11 @@ int launch_attend_bwd(const void *q, const void *k, const void *v, const int32_t
                       const float *w, int ks, const void *dout, const bra::BwdGeom &g,
                       size_t smem, float *dq, float *dk, float *dv, float *dw, float *db,
                       cudaStream_t s) {
-  auto kern = bra::bra_attend_bwd_kernel<T>;
+  // head dimension 32 and 64 keys a query (the stage-1 to stage-3 shapes)
+  // fixed at compile time where they hold
+  auto kern = g.d == 32 && g.nk == 64 ? bra::bra_attend_bwd_kernel<T, 32, 64>
+              : g.d == 32             ? bra::bra_attend_bwd_kernel<T, 32, 0>
+                                      : bra::bra_attend_bwd_kernel<T, 0, 0>;
   if (allow_smem(reinterpret_cast<const void *>(kern), smem) != cudaSuccess)
     return BRA_ERR_CUDA;
   const unsigned grid = (unsigned)((size_t)B * g.R * g.heads);
